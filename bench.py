@@ -1,0 +1,510 @@
+"""Benchmark of the lat_attn hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra] [--no-cpu]
+
+A step is one pass of the attention hot path over one batch of synthetic input.  The
+headline workload is the Qwen3-0.6B-shaped bf16 prefill (batch 8, 512 tokens, 16 query
+heads, 8 KV heads, head_dim 64, causal) read with row strides from one packed
+[4096, 2048] QKV buffer.  Each timed step is bracketed by CUDA events on the launching
+stream, with a 256 MiB write between steps so every step starts with a cold L2.
+
+`value` is TFLOP/s of algorithmic work (4*D FLOPs per visible query-key pair per head).
+`e2e` repeats the step through the C ABI from pinned host buffers, with the QKV upload
+and the output/lse download inside the timed region.  `roofline` rates the prefill kernel
+against the HBM roofline (this workload's arithmetic intensity is below the ridge point).
+`workloads` adds the other named shapes (Gemma-4 sliding/global prefill, both decode
+shapes), each rated against its own roofline.  `cpu_baseline` is the fp64 oracle timed on
+the host cores.  With --impl reference the oracle itself is the timed arm.
+
+Multi-GPU runs (torchrun) are independent replicas of the same workload (the path has no
+exchange step); every rank times its own steps and the slowest rank sets the time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "GQA attention prefill TFLOP/s and decode KV GB/s, % of GB300 roofline"
+HEADLINE = "qwen3_0.6b_prefill"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_pairs(S, L, causal, window):
+    """Number of (query row, key) pairs the mask leaves visible, per (batch, head)."""
+    i = np.arange(S, dtype=np.int64)
+    p = i + (L - S)
+    hi = np.minimum(L, p + 1) if causal else np.full(S, L, dtype=np.int64)
+    lo = np.maximum(0, p - window + 1) if window > 0 else np.zeros(S, dtype=np.int64)
+    return int(np.maximum(hi - lo, 0).sum())
+
+
+def prefill_work(wl):
+    pairs = visible_pairs(wl.S, wl.L, wl.causal, wl.window)
+    flops = 4.0 * wl.D * wl.Hq * wl.B * pairs
+    es = 2 if wl.dtype == "bf16" else 4
+    bytes_ = (wl.B * wl.S * wl.Hq * wl.D * es * 2          # Q read, out written
+              + 2 * wl.B * wl.L * wl.Hkv * wl.D * es        # K, V read once
+              + wl.B * wl.S * wl.Hq * 4)                    # lse written
+    return flops, float(bytes_), pairs
+
+
+def decode_work(wl, kv_lens):
+    es = 2 if wl.dtype == "bf16" else 4
+    keys = int(sum(min(int(n), wl.window) if wl.window > 0 else int(n) for n in kv_lens))
+    kv_bytes = keys * wl.Hkv * wl.D * 2 * es
+    bytes_ = kv_bytes + wl.B * wl.Hq * wl.D * es * 2 + wl.B * wl.Hq * 4
+    flops = 4.0 * wl.D * wl.Hq * keys
+    return flops, float(bytes_), keys
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gqa_attention_lat_gb300", "csrc")
+    for n in names:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(profile_name, src_names):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on the
+    current kernel source (the summary records the source hash); else None."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash(src_names):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the GPU is busy."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.idx = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+class Flusher:
+    def __init__(self, device):
+        self.buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_steps(fn, steps, flush, stream):
+    """Run `fn` `steps` times, L2 flushed before each; returns per-step ms (CUDA events
+    recorded on the stream the kernels run on)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        flush()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+class PrefillStep:
+    def __init__(self, wl, device):
+        from gqa_attention_lat_gb300 import binding
+        self.b = binding
+        self.wl = wl
+        self.inp = W.prefill_inputs(wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, dtype=wl.dtype,
+                                    device=device, packed=wl.packed, k_mul=wl.k_mul)
+        self.out = torch.empty((wl.B * wl.S, wl.Hq * wl.D), dtype=W.torch_dtype(wl.dtype),
+                               device=device)
+        self.lse = torch.empty((wl.B * wl.S, wl.Hq), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.dt = binding.LAT_BF16 if wl.dtype == "bf16" else binding.LAT_F32
+
+    def __call__(self, q=None, k=None, v=None):
+        i, wl = self.inp, self.wl
+        q = i.q if q is None else q
+        k = i.k if k is None else k
+        v = i.v if v is None else v
+        self.b.lat_attn_prefill(self.dt, q, i.q.stride(0), k, i.k.stride(0), v, i.v.stride(0),
+                                self.out, self.out.stride(0), self.lse, wl.B, wl.S, wl.L, wl.Hq,
+                                wl.Hkv, wl.D, wl.causal, wl.window, wl.scale, self.status)
+
+    def check_status(self):
+        st = int(self.status.item())
+        if st != 0:
+            raise RuntimeError("device status %s" % self.b.lat_status_string(st))
+
+
+class DecodeStep:
+    def __init__(self, wl, device):
+        from gqa_attention_lat_gb300 import binding
+        self.b = binding
+        self.wl = wl
+        self.di = W.decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.L, kv_lens=wl.kv_lens,
+                                  dtype=wl.dtype, device=device, nan_fill=True)
+        self.dt = binding.LAT_BF16 if wl.dtype == "bf16" else binding.LAT_F32
+        self.nbytes = binding.lat_attn_decode_workspace_size(self.dt, wl.B, wl.Hq, wl.Hkv, wl.D,
+                                                             wl.L)
+        self.ws = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+        self.out = torch.empty((wl.B, wl.Hq * wl.D), dtype=W.torch_dtype(wl.dtype), device=device)
+        self.lse = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        d, wl = self.di, self.wl
+        self.b.lat_attn_decode(self.dt, d.q, d.q.stride(0), d.k_cache, d.v_cache, wl.Hkv * wl.D,
+                               wl.D, wl.L * wl.Hkv * wl.D, d.kv_lens, wl.L, self.out,
+                               self.out.stride(0), self.lse, wl.B, wl.Hq, wl.Hkv, wl.D,
+                               wl.window, wl.scale, self.ws, self.nbytes, self.status)
+
+    def check_status(self):
+        st = int(self.status.item())
+        if st != 0:
+            raise RuntimeError("device status %s" % self.b.lat_status_string(st))
+
+
+def measure_extra(device, flush, stream, peaks, reps=10):
+    """The other named workloads, each against its own roofline."""
+    res = {}
+    for name in ("gemma4_sliding_prefill", "gemma4_global_prefill"):
+        wl = W.WORKLOADS[name]
+        step = PrefillStep(wl, device)
+        for _ in range(3):
+            step()
+        ms = time_steps(step, reps, flush, stream)
+        step.check_status()
+        flops, bytes_, _ = prefill_work(wl)
+        t = statistics.median(ms) / 1e3
+        tf = flops / t / 1e12
+        res[name] = {"kind": "prefill", "ms": statistics.median(ms), "tflops": tf,
+                     "bound": "tensor", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                     "gflop": flops / 1e9}
+        del step
+        torch.cuda.empty_cache()
+    for name in ("decode_b32_h32_kv8_d128", "gemma4_global_decode"):
+        wl = W.WORKLOADS[name]
+        step = DecodeStep(wl, device)
+        for _ in range(3):
+            step()
+        ms = time_steps(step, reps, flush, stream)
+        step.check_status()
+        flops, bytes_, keys = decode_work(wl, step.di.kv_lens.cpu().tolist())
+        t = statistics.median(ms) / 1e3
+        gbs = bytes_ / t / 1e9
+        res[name] = {"kind": "decode", "ms": statistics.median(ms), "gbs": gbs, "bound": "hbm",
+                     "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "mbytes": bytes_ / 1e6,
+                     "tflops": flops / t / 1e12}
+        del step
+        torch.cuda.empty_cache()
+    return res
+
+
+def e2e_measure(step, steps, stream):
+    """Host buffers through the C ABI: upload QKV from pinned memory, run, download."""
+    wl, inp = step.wl, step.inp
+    parent = inp.packed if inp.packed is not None else None
+    if parent is None:
+        raise RuntimeError("e2e leg expects the packed QKV workload")
+    host_in = torch.empty(parent.shape, dtype=parent.dtype, pin_memory=True)
+    host_in.copy_(parent.cpu())
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype, pin_memory=True)
+    dev_in = torch.empty_like(parent)
+    qw, kw = wl.Hq * wl.D, wl.Hkv * wl.D
+    q, k, v = dev_in[:, :qw], dev_in[:, qw:qw + kw], dev_in[:, qw + kw:]
+
+    def one():
+        dev_in.copy_(host_in, non_blocking=True)
+        step(q, k, v)
+        host_out.copy_(step.out, non_blocking=True)
+        host_lse.copy_(step.lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------------------ CPU arm
+
+def oracle_pass(wl, inp_cpu, threads, rows=None):
+    import oracle
+    return oracle.prefill(inp_cpu.heads("q"), inp_cpu.heads("k"), inp_cpu.heads("v"),
+                          causal=wl.causal, window=wl.window, scale=wl.scale, rows=rows,
+                          threads=threads)
+
+
+def cpu_baseline(wl, seconds=8.0):
+    """The oracle as it stands, on the host cores, over whole passes of the workload
+    (repeated until `seconds` of CPU time have run)."""
+    import oracle
+    oracle.build_library()
+    threads = oracle.default_threads()
+    inp = W.prefill_inputs(wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, dtype=wl.dtype, device="cpu",
+                           packed=wl.packed, k_mul=wl.k_mul)
+    flops, _, _ = prefill_work(wl)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(wl, inp, threads)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops * n / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": "%d full passes of %s (fp64 oracle, %d threads, %.1f s)"
+            % (n, wl.name, threads, dt)}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle is the timed arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build_library()
+    wl = W.WORKLOADS[args.workload]
+    threads = oracle.default_threads()
+    inp = W.prefill_inputs(wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, dtype=wl.dtype, device="cpu",
+                           packed=wl.packed, k_mul=wl.k_mul)
+    flops, _, _ = prefill_work(wl)
+    for _ in range(args.warmup):
+        oracle_pass(wl, inp, threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_pass(wl, inp, threads)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms / 1e3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": "each step is one full pass of %s" % wl.name},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    return {"workload": "%s: B%d S%d Hq%d Hkv%d D%d %s%s %s%s" % (
+        wl.name, wl.B, wl.S, wl.Hq, wl.Hkv, wl.D, "causal" if wl.causal else "full",
+        " window %d" % wl.window if wl.window else "", wl.dtype,
+        ", packed QKV [%d, %d]" % (wl.B * wl.S, (wl.Hq + 2 * wl.Hkv) * wl.D) if wl.packed else ""),
+        "batch": wl.B, "seq_len": wl.S, "kv_len": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
+        "head_dim": wl.D, "causal": wl.causal, "window": wl.window,
+        "l2": "flushed before every timed step (256 MiB write)",
+        "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    from gqa_attention_lat_gb300.build import build_library
+    if rank == 0 or world == 1:
+        build_library()
+    if dist is not None:
+        dist.barrier()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_src = load_peaks()
+    wl = W.WORKLOADS[args.workload]
+    if wl.kind != "prefill" or wl.dtype != "bf16":
+        raise SystemExit("the headline workload must be a bf16 prefill")
+    flush = Flusher(device)
+    step = PrefillStep(wl, device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    step.check_status()
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms_steps = time_steps(step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    step.check_status()
+    ms_total = sum(ms_steps)
+    if dist is not None:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / args.steps
+    flops, alg_bytes, pairs = prefill_work(wl)
+    value = flops * world / (ms_per_step / 1e3) / 1e12
+
+    e2e_ms, h2d, d2h = e2e_measure(step, args.steps, stream)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops * world / (e2e_ms / 1e3) / 1e12
+
+    extra = None
+    if not args.no_extra:
+        del step
+        torch.cuda.empty_cache()
+        extra = measure_extra(device, flush, stream, peaks)
+    clocks = sampler.stop()
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and world == 1:
+        cpu = cpu_baseline(wl)
+
+    kernel_ms = statistics.mean(ms_steps)
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    traffic = profile_traffic("prefill_tc_qwen3_0.6b_prefill.md",
+                              ["prefill_tc.cu", "device_common.cuh", "kernels.h"])
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": workload_config(wl),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "prefill_tc_kernel<64>", "peak_source": peak_src,
+                     "algorithmic_bytes": alg_bytes,
+                     "tensor_frac": (flops / (kernel_ms / 1e3) / 1e12) / peaks["bf16_tflops"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "workloads": extra,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,321 @@
+// api.cu — the C ABI declared in include/lat_attn.h: argument validation, launch planning,
+// tensor-map encoding and dispatch to the kernels.  No allocation, no global mutable state
+// (the driver entry point for tensor-map encoding is resolved once and then read-only).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "lat_attn.h"
+#include "lat_attn_testing.h"
+
+namespace {
+
+bool supported_head_dim(int d) { return d == 64 || d == 80 || d == 128 || d == 256 || d == 512; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 4-D bf16 map over (head-dim d, head, row, batch) with a [64, 1, box_rows, 1] box and
+// 128-byte swizzle.  Columns past head_dim and rows past `rows` read as zero.
+bool make_head_map(CUtensorMap *m, const void *base, int head_dim, int heads, int rows,
+                   int batch, int64_t row_stride, int box_rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows,
+                                (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)row_stride * 2,
+                                   (cuuint64_t)row_stride * 2 * (cuuint64_t)rows};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int current_sm_count(int *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s per CTA
+
+lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k, int64_t k_rs,
+                        const void *v, int64_t v_rs, void *out, int64_t out_rs, float *lse,
+                        int batch, int seq_len, int kv_len, int n_heads, int n_kv_heads,
+                        int head_dim, int causal, int window, float scale, int32_t *status,
+                        void *stream, uint64_t timeout_ns, int skip_kv_load) {
+    if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
+    if (batch < 0 || seq_len < 0 || kv_len < seq_len || n_heads <= 0 || n_kv_heads <= 0 ||
+        n_heads % n_kv_heads != 0)
+        return LAT_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return LAT_ERR_UNSUPPORTED;
+    if (!isfinite(scale)) return LAT_ERR_INVALID_ARG;
+    if (batch == 0 || seq_len == 0) return LAT_OK;
+    if (!q || !k || !v || !out) return LAT_ERR_INVALID_ARG;
+    if (q_rs < (int64_t)n_heads * head_dim || out_rs < (int64_t)n_heads * head_dim ||
+        k_rs < (int64_t)n_kv_heads * head_dim || v_rs < (int64_t)n_kv_heads * head_dim)
+        return LAT_ERR_INVALID_ARG;
+    if (batch > 65535 || (seq_len + 127) / 128 > 65535) return LAT_ERR_UNSUPPORTED;
+    if (window < 0) window = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (dt == LAT_F32) {
+        lat::RowAttnArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.q_rs = q_rs;
+        a.k = static_cast<const float *>(k);
+        a.v = static_cast<const float *>(v);
+        a.k_seq = (int64_t)kv_len * k_rs;
+        a.k_row = k_rs;
+        a.k_head = head_dim;
+        a.v_seq = (int64_t)kv_len * v_rs;
+        a.v_row = v_rs;
+        a.v_head = head_dim;
+        a.out = static_cast<float *>(out);
+        a.out_rs = out_rs;
+        a.lse = lse;
+        a.batch = batch;
+        a.seq_len = seq_len;
+        a.kv_len = kv_len;
+        a.n_heads = n_heads;
+        a.n_kv_heads = n_kv_heads;
+        a.head_dim = head_dim;
+        a.causal = causal != 0;
+        a.window = window;
+        a.scale = scale;
+        a.kv_lens = nullptr;
+        a.max_kv_len = kv_len;
+        a.status = status;
+        return lat::launch_row_attention_f32(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
+    }
+
+    // bf16: tensor-memory-access reads need 16-byte aligned bases and row strides
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || q_rs % 8 ||
+        k_rs % 8 || v_rs % 8 || out_rs % 8)
+        return LAT_ERR_INVALID_ARG;
+    lat::PrefillTcArgs a{};
+    const int bn = lat::prefill_tc_block_n(head_dim);
+    if (!make_head_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, 128) ||
+        !make_head_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, k_rs, bn) ||
+        !make_head_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, v_rs, bn))
+        return LAT_ERR_CUDA;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.out_rs = out_rs;
+    a.lse = lse;
+    a.batch = batch;
+    a.seq_len = seq_len;
+    a.kv_len = kv_len;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.causal = causal != 0;
+    a.window = window;
+    a.scale_log2 = scale * kLog2e;
+    a.status = status;
+    a.timeout_ns = timeout_ns;
+    a.test_skip_kv_load = skip_kv_load;
+    return lat::launch_prefill_tc(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lat_status_string(lat_status st) {
+    switch (st) {
+        case LAT_OK: return "LAT_OK";
+        case LAT_ERR_INVALID_ARG: return "LAT_ERR_INVALID_ARG";
+        case LAT_ERR_UNSUPPORTED: return "LAT_ERR_UNSUPPORTED";
+        case LAT_ERR_WORKSPACE: return "LAT_ERR_WORKSPACE";
+        case LAT_ERR_CUDA: return "LAT_ERR_CUDA";
+        case LAT_ERR_BOUNDS: return "LAT_ERR_BOUNDS";
+        case LAT_ERR_TIMEOUT: return "LAT_ERR_TIMEOUT";
+    }
+    return "LAT_ERR_UNKNOWN";
+}
+
+lat_status lat_attn_prefill(lat_dtype dt, const void *q, int64_t q_rs, const void *k,
+                            int64_t k_rs, const void *v, int64_t v_rs, void *out,
+                            int64_t out_rs, float *lse, int batch, int seq_len, int kv_len,
+                            int n_heads, int n_kv_heads, int head_dim, int causal, int window,
+                            float scale, int32_t *status, void *stream) {
+    return prefill_impl(dt, q, q_rs, k, k_rs, v, v_rs, out, out_rs, lse, batch, seq_len,
+                        kv_len, n_heads, n_kv_heads, head_dim, causal, window, scale, status,
+                        stream, kDefaultTimeoutNs, 0);
+}
+
+lat_status lat_test_prefill_timeout(const void *q, int64_t q_rs, const void *k, int64_t k_rs,
+                                    const void *v, int64_t v_rs, void *out, int64_t out_rs,
+                                    int batch, int seq_len, int n_heads, int n_kv_heads,
+                                    int head_dim, uint64_t timeout_ns, int32_t *status,
+                                    void *stream) {
+    return prefill_impl(LAT_BF16, q, q_rs, k, k_rs, v, v_rs, out, out_rs, nullptr, batch,
+                        seq_len, seq_len, n_heads, n_kv_heads, head_dim, 1, 0, 0.125f, status,
+                        stream, timeout_ns, 1);
+}
+
+size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int n_kv_heads,
+                                      int head_dim, int max_kv_len) {
+    if (dt == LAT_F32) return 0;
+    if (dt != LAT_BF16 || batch < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
+        n_heads % n_kv_heads != 0 || !supported_head_dim(head_dim) || max_kv_len < 0)
+        return 0;
+    int sms = 0;
+    if (!current_sm_count(&sms)) return 0;
+    lat::DecodePlan plan;
+    if (!lat::plan_decode_bf16(batch, n_heads, n_kv_heads, head_dim, max_kv_len, 0, sms, &plan))
+        return 0;
+    return plan.total_bytes;
+}
+
+lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
+                           const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,
+                           int64_t cache_seq_stride, const int32_t *kv_lens, int max_kv_len,
+                           void *out, int64_t out_rs, float *lse, int batch, int n_heads,
+                           int n_kv_heads, int head_dim, int window, float scale,
+                           void *workspace, size_t workspace_bytes, int32_t *status,
+                           void *stream) {
+    if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
+    if (batch < 0 || max_kv_len < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
+        n_heads % n_kv_heads != 0)
+        return LAT_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return LAT_ERR_UNSUPPORTED;
+    if (!isfinite(scale)) return LAT_ERR_INVALID_ARG;
+    if (batch == 0) return LAT_OK;
+    if (!q || !k_cache || !v_cache || !kv_lens || !out) return LAT_ERR_INVALID_ARG;
+    if (q_rs < (int64_t)n_heads * head_dim || out_rs < (int64_t)n_heads * head_dim ||
+        cache_rs <= 0 || cache_head_stride <= 0 || cache_seq_stride <= 0)
+        return LAT_ERR_INVALID_ARG;
+    if (batch > 65535) return LAT_ERR_UNSUPPORTED;
+    if (window < 0) window = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (dt == LAT_F32) {
+        lat::RowAttnArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.q_rs = q_rs;
+        a.k = static_cast<const float *>(k_cache);
+        a.v = static_cast<const float *>(v_cache);
+        a.k_seq = a.v_seq = cache_seq_stride;
+        a.k_row = a.v_row = cache_rs;
+        a.k_head = a.v_head = cache_head_stride;
+        a.out = static_cast<float *>(out);
+        a.out_rs = out_rs;
+        a.lse = lse;
+        a.batch = batch;
+        a.seq_len = 1;
+        a.kv_len = 0;
+        a.n_heads = n_heads;
+        a.n_kv_heads = n_kv_heads;
+        a.head_dim = head_dim;
+        a.causal = 1;
+        a.window = window;
+        a.scale = scale;
+        a.kv_lens = kv_lens;
+        a.max_kv_len = max_kv_len;
+        a.status = status;
+        return lat::launch_row_attention_f32(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
+    }
+
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || q_rs % 8 ||
+        cache_rs % 8 || cache_head_stride % 8 || cache_seq_stride % 8)
+        return LAT_ERR_INVALID_ARG;
+    int sms = 0;
+    if (!current_sm_count(&sms)) return LAT_ERR_CUDA;
+    lat::DecodePlan plan;
+    if (!lat::plan_decode_bf16(batch, n_heads, n_kv_heads, head_dim, max_kv_len, window, sms,
+                               &plan))
+        return LAT_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < plan.total_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return LAT_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    lat::DecodeArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.q_rs = q_rs;
+    a.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
+    a.v_cache = static_cast<const __nv_bfloat16 *>(v_cache);
+    a.cache_rs = cache_rs;
+    a.cache_head = cache_head_stride;
+    a.cache_seq = cache_seq_stride;
+    a.kv_lens = kv_lens;
+    a.max_kv_len = max_kv_len;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.out_rs = out_rs;
+    a.lse = lse;
+    a.batch = batch;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.window = window;
+    a.scale_log2 = scale * kLog2e;
+    a.part_o = reinterpret_cast<float *>(ws);
+    a.part_lse = reinterpret_cast<float *>(ws + plan.part_o_bytes);
+    a.counters = reinterpret_cast<int32_t *>(ws + plan.part_o_bytes + plan.part_lse_bytes);
+    a.max_splits = plan.max_splits;
+    a.chunk = plan.chunk;
+    a.status = status;
+    return lat::launch_decode_bf16(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
+}
+
+lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
+                         int64_t cache_head_stride, int64_t cache_seq_stride, int capacity,
+                         const void *k_new, const void *v_new, int64_t new_rs,
+                         const int32_t *pos, int n_new, int batch, int n_kv_heads,
+                         int head_dim, int32_t *status, void *stream) {
+    if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
+    if (batch < 0 || n_new < 0 || capacity < 0 || n_kv_heads <= 0) return LAT_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return LAT_ERR_UNSUPPORTED;
+    if (batch == 0 || n_new == 0) return LAT_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !pos) return LAT_ERR_INVALID_ARG;
+    if (cache_rs <= 0 || cache_head_stride <= 0 || cache_seq_stride <= 0 ||
+        new_rs < (int64_t)n_kv_heads * head_dim)
+        return LAT_ERR_INVALID_ARG;
+    lat::AppendArgs a{};
+    a.k_cache = static_cast<char *>(k_cache);
+    a.v_cache = static_cast<char *>(v_cache);
+    a.k_new = static_cast<const char *>(k_new);
+    a.v_new = static_cast<const char *>(v_new);
+    a.cache_rs = cache_rs;
+    a.cache_head = cache_head_stride;
+    a.cache_seq = cache_seq_stride;
+    a.new_rs = new_rs;
+    a.pos = pos;
+    a.capacity = capacity;
+    a.n_new = n_new;
+    a.batch = batch;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.elem_bytes = dt == LAT_F32 ? 4 : 2;
+    a.status = status;
+    return lat::launch_kv_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? LAT_OK
+               : LAT_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// kernels.h — internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Host-only declarations; every argument has been validated by the
+// caller before a launcher runs.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lat {
+
+// ---------------------------------------------------------------- KV-cache append
+struct AppendArgs {
+    char *k_cache, *v_cache;          // byte pointers
+    const char *k_new, *v_new;
+    int64_t cache_rs, cache_head, cache_seq, new_rs;  // element strides
+    const int32_t *pos;
+    int capacity, n_new, batch, n_kv_heads, head_dim, elem_bytes;
+    int32_t *status;
+};
+cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------- fp32 row kernel
+// One warp per (query row, query head); used for every fp32 prefill and decode.
+// Element (b, j, hk, d) of K is k[b*k_seq + j*k_row + hk*k_head + d] (V alike);
+// in decode mode (kv_lens != nullptr) seq_len is 1 and sequence b has kv_lens[b] keys.
+struct RowAttnArgs {
+    const float *q;
+    int64_t q_rs;
+    const float *k, *v;
+    int64_t k_seq, k_row, k_head, v_seq, v_row, v_head;
+    float *out;
+    int64_t out_rs;
+    float *lse;
+    int batch, seq_len, kv_len, n_heads, n_kv_heads, head_dim, causal, window;
+    float scale;
+    const int32_t *kv_lens;
+    int max_kv_len;
+    int32_t *status;
+};
+cudaError_t launch_row_attention_f32(const RowAttnArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------- bf16 split-KV decode
+struct DecodeArgs {
+    const __nv_bfloat16 *q;
+    int64_t q_rs;
+    const __nv_bfloat16 *k_cache, *v_cache;
+    int64_t cache_rs, cache_head, cache_seq;
+    const int32_t *kv_lens;
+    int max_kv_len;
+    __nv_bfloat16 *out;
+    int64_t out_rs;
+    float *lse;
+    int batch, n_heads, n_kv_heads, head_dim, window;
+    float scale_log2;   // scale * log2(e): scores are exponentiated with exp2
+    // split-KV scratch: partial outputs, partial lse and arrival counters
+    float *part_o;      // [batch, n_heads, max_splits, head_dim]
+    float *part_lse;    // [batch, n_heads, max_splits]
+    int32_t *counters;  // [batch, n_kv_heads, head_blocks]
+    int max_splits, chunk;
+    int32_t *status;
+};
+struct DecodePlan {
+    int head_blocks, max_splits, chunk;
+    size_t part_o_bytes, part_lse_bytes, counter_bytes, total_bytes;
+};
+// Chooses the split size and the scratch layout; false when the shape is not built.
+bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
+                      int window, int num_sms, DecodePlan *plan);
+cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------- bf16 tensor-core prefill
+struct PrefillTcArgs {
+    CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps (d, head, row, batch), 128-byte swizzle
+    __nv_bfloat16 *out;
+    int64_t out_rs;
+    float *lse;
+    int batch, seq_len, kv_len, n_heads, n_kv_heads, head_dim, causal, window;
+    float scale_log2;              // scale * log2(e)
+    int32_t *status;
+    uint64_t timeout_ns;
+    int test_skip_kv_load;         // test hook: never load KV tile 0 (forces a timeout)
+};
+int prefill_tc_block_n(int head_dim);        // keys per KV tile for this head_dim
+cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s);
+
+}  // namespace lat

@@ -1,0 +1,104 @@
+// row_attention_f32.cu — exact-fp32 attention on the CUDA cores, one warp per
+// (query row, query head).  Serves every LAT_F32 call (prefill and decode).
+//
+// The arithmetic is the row-wise online softmax of the lattice-inference DESIGN page
+// ("Current Design": fused attention, online softmax in registers): keys are visited in
+// order, each score s = scale * q.k is reduced across the warp, and the running maximum
+// m, normaliser l and output accumulator o are updated as
+//   m' = max(m, s),  l' = l*e^(m-m') + e^(s-m'),  o' = o*e^(m-m') + e^(s-m')*v.
+// fp32 inputs keep fp32 products (no tf32), so the result stays within ~1e-6 of fp64.
+// Lane `lane` owns head dimensions d = lane + 32*t, t < NT.
+#include <math.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace lat {
+
+template <int NT>
+__global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t unit = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int64_t n_units = (int64_t)a.batch * a.seq_len * a.n_heads;
+    if (unit >= n_units) return;
+    const int h = (int)(unit % a.n_heads);
+    const int64_t r = unit / a.n_heads;  // flattened query row b*seq_len + i
+    const int b = (int)(r / a.seq_len), i = (int)(r % a.seq_len);
+    const int D = a.head_dim;
+
+    int L = a.kv_len;
+    if (a.kv_lens != nullptr) {
+        L = a.kv_lens[b];
+        if (L < 0 || L > a.max_kv_len) {
+            if (lane == 0 && h == 0) report_status(a.status, kErrBounds);
+            return;
+        }
+    }
+    const int p = i + (L - a.seq_len);                 // absolute query position
+    const int hi = a.causal ? min(L, p + 1) : L;       // causal: keys j <= p
+    const int lo = a.window > 0 ? max(0, p - a.window + 1) : 0;  // window: p - j < W
+    const int hk = h / (a.n_heads / a.n_kv_heads);
+
+    const float *qrow = a.q + r * a.q_rs + (int64_t)h * D;
+    float qv[NT], o[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int d = lane + 32 * t;
+        qv[t] = d < D ? qrow[d] : 0.f;
+        o[t] = 0.f;
+    }
+    const float *kb = a.k + (int64_t)b * a.k_seq + (int64_t)hk * a.k_head;
+    const float *vb = a.v + (int64_t)b * a.v_seq + (int64_t)hk * a.v_head;
+    float m = -INFINITY, l = 0.f;
+    for (int j = lo; j < hi; ++j) {
+        const float *kr = kb + (int64_t)j * a.k_row;
+        float part = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int d = lane + 32 * t;
+            if (d < D) part = fmaf(qv[t], kr[d], part);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        const float s = part * a.scale;
+        const float m_new = fmaxf(m, s);
+        const float corr = expf(m - m_new);
+        const float w = expf(s - m_new);
+        l = l * corr + w;
+        const float *vr = vb + (int64_t)j * a.v_row;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int d = lane + 32 * t;
+            if (d < D) o[t] = o[t] * corr + w * vr[d];
+        }
+        m = m_new;
+    }
+    const bool empty = hi <= lo;
+    const float inv_l = empty ? 0.f : 1.f / l;
+    float *orow = a.out + r * a.out_rs + (int64_t)h * D;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int d = lane + 32 * t;
+        if (d < D) orow[d] = o[t] * inv_l;
+    }
+    if (a.lse != nullptr && lane == 0)
+        a.lse[r * a.n_heads + h] = empty ? -INFINITY : m + logf(l);
+}
+
+cudaError_t launch_row_attention_f32(const RowAttnArgs &a, cudaStream_t s) {
+    const int64_t n_units = (int64_t)a.batch * a.seq_len * a.n_heads;
+    if (n_units == 0) return cudaSuccess;
+    const int64_t blocks = (n_units + 3) / 4;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    switch (a.head_dim) {
+        case 64: row_attention_f32_kernel<2><<<(unsigned)blocks, 128, 0, s>>>(a); break;
+        case 80: row_attention_f32_kernel<3><<<(unsigned)blocks, 128, 0, s>>>(a); break;
+        case 128: row_attention_f32_kernel<4><<<(unsigned)blocks, 128, 0, s>>>(a); break;
+        case 256: row_attention_f32_kernel<8><<<(unsigned)blocks, 128, 0, s>>>(a); break;
+        case 512: row_attention_f32_kernel<16><<<(unsigned)blocks, 128, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lat

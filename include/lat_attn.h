@@ -1,0 +1,165 @@
+/*
+ * lat_attn.h — fused grouped-query attention for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation is scaled-dot-product softmax attention with grouped-query heads:
+ *
+ *   for query row i of sequence b and query head h (G = n_heads / n_kv_heads,
+ *   KV head hk = h / G, query position p = i + (kv_len - seq_len)):
+ *     s_j   = scale * sum_d q[b,i,h,d] * k[b,j,hk,d]       over visible keys j
+ *     out   = sum_j exp(s_j - m) * v[b,j,hk,:] / Z,   m = max_j s_j,  Z = sum_j exp(s_j - m)
+ *     lse   = m + ln Z                                  (natural log)
+ *
+ * This is the row-wise attention of the larql "Inference Engine" page (section
+ * "BLAS-Fused Attention": scores from K times Q, head scale, softmax, V^T times the
+ * weights, GQA with any Q/KV ratio, causal masking built in), computed the way the
+ * lattice-inference DESIGN page's fused Metal kernel does it ("Current Design":
+ * fused attention with online softmax in registers, head_dim a compile-time
+ * specialisation).  Visibility of key j from position p:
+ *   causal != 0  ->  j <= p
+ *   window  > 0  ->  p - j < window        (window keys including the query's own;
+ *                                          Gemma 4 sliding layers use 1024, hf2q
+ *                                          "Current Inference Path" page, section 2)
+ * A row with no visible key gets out = 0 and lse = -inf.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers are caller-owned DEVICE memory unless stated otherwise.  The library
+ *   allocates nothing; scratch space is passed in by the caller.
+ * - Strides and row strides are in ELEMENTS of the call's dtype.  Within a row the
+ *   heads of a tensor sit side by side with stride head_dim, so Q, K and V can be
+ *   column slices of one packed QKV buffer read with the parent's row stride (the
+ *   rlx-metal DESIGN page, "Cross-crate contract": per-tensor q/k/v row strides let
+ *   attention read straight from the fused QKV output).
+ * - head_dim is one of 64, 80, 128, 256, 512 (the Qwen3 and Gemma 4 head sizes named
+ *   by the lattice-inference DESIGN page's compatibility matrix and the hf2q page);
+ *   anything else returns LAT_ERR_UNSUPPORTED.
+ * - n_heads % n_kv_heads != 0 returns LAT_ERR_INVALID_ARG (the same rule as
+ *   INV-3 on the lattice-inference DESIGN page, without its CPU fallback: there is
+ *   no fallback here, ever).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *   stream).  Errors found on the host return at once and launch nothing.  Errors
+ *   found on the device are written to `*status` (a device int32, nullable; it is
+ *   set from 0 to the first error code seen and never cleared by the library);
+ *   read it after synchronising.
+ * - No global mutable state; calls on different streams are independent as long as
+ *   their output and scratch buffers do not overlap.
+ */
+#ifndef LAT_ATTN_H
+#define LAT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { LAT_F32 = 0, LAT_BF16 = 1 } lat_dtype;
+
+typedef enum {
+    LAT_OK = 0,
+    LAT_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride, bad ratio   */
+    LAT_ERR_UNSUPPORTED = 2, /* head_dim or dtype combination not built              */
+    LAT_ERR_WORKSPACE = 3,   /* decode workspace missing or too small                */
+    LAT_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, attribute) */
+    LAT_ERR_BOUNDS = 5,      /* device: a cache position or kv_len out of range       */
+    LAT_ERR_TIMEOUT = 6      /* device: a bounded pipeline wait ran out; kernel quit   */
+} lat_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *lat_status_string(lat_status s);
+
+/*
+ * lat_attn_prefill — attention for seq_len query rows per sequence over kv_len keys.
+ *
+ * Layout (r = row index):
+ *   q   element (b,i,h,d) at q[(b*seq_len + i)*q_rs + h*head_dim + d]
+ *   k   element (b,j,hk,d) at k[(b*kv_len + j)*k_rs + hk*head_dim + d]; v likewise with v_rs
+ *   out element (b,i,h,d) at out[(b*seq_len + i)*out_rs + h*head_dim + d], dtype dt
+ *   lse (nullable) fp32 at lse[(b*seq_len + i)*n_heads + h]
+ * kv_len >= seq_len >= 0 (kv_len > seq_len is a chunk of new queries appended after
+ * kv_len - seq_len earlier keys).  dt = LAT_BF16 runs on the tensor cores
+ * (bf16 operands, fp32 accumulation, one bf16 rounding of the output); dt = LAT_F32
+ * runs exact fp32 arithmetic on the CUDA cores.
+ * For LAT_BF16, q, k, v and out must be 16-byte aligned and q_rs, k_rs, v_rs, out_rs
+ * multiples of 8 (the tensor-memory-access unit reads 16-byte aligned rows and the
+ * epilogue writes 16-byte vectors), else LAT_ERR_INVALID_ARG.
+ * `out` must not overlap q, k or v.
+ */
+lat_status lat_attn_prefill(lat_dtype dt, const void *q, int64_t q_rs, const void *k,
+                            int64_t k_rs, const void *v, int64_t v_rs, void *out,
+                            int64_t out_rs, float *lse, int batch, int seq_len, int kv_len,
+                            int n_heads, int n_kv_heads, int head_dim, int causal,
+                            int window, float scale, int32_t *status, void *stream);
+
+/*
+ * lat_attn_decode_workspace_size — bytes of scratch lat_attn_decode needs for these
+ * sizes (its split-KV partial results and merge counters).  Returns 0 for sizes the
+ * library rejects.
+ */
+size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int n_kv_heads,
+                                      int head_dim, int max_kv_len);
+
+/*
+ * lat_attn_decode — one query token per sequence against an in-place KV cache.
+ *
+ * The decode step of the hf2q "Current Inference Path" page (section 3: attention at
+ * seq_len 1 over the KV cache, right after the cache append).  The query of
+ * sequence b sits at position kv_lens[b] - 1 and reads cached keys
+ * max(0, kv_lens[b] - window) .. kv_lens[b] - 1 (all of 0 .. kv_lens[b]-1 when
+ * window <= 0), so it equals the last row of a causal prefill over those keys.
+ *
+ * Layout:
+ *   q      element (b,h,d) at q[b*q_rs + h*head_dim + d]
+ *   caches element (b,j,hk,d) at cache[b*cache_seq_stride + j*cache_rs +
+ *                                      hk*cache_head_stride + d]   (k_cache and v_cache)
+ *          token-major [B, cap, Hkv*D]: cache_rs = Hkv*D, cache_head_stride = D;
+ *          head-major  [B, Hkv, cap, D]: cache_rs = D, cache_head_stride = cap*D
+ *          (the hf2q target page's per-layer cache [1, kv_heads, max_cache, head_dim]).
+ *   kv_lens device int32 [batch], each in [0, max_kv_len]; a value outside that
+ *          range sets *status = LAT_ERR_BOUNDS and that row's output is left unwritten.
+ *   out    element (b,h,d) at out[b*out_rs + h*head_dim + d], dtype dt
+ *   lse    nullable fp32 [batch, n_heads]
+ * max_kv_len is a host-side upper bound used to size the launch.  Cache slots at or
+ * past kv_lens[b] are never read (they may hold anything, NaN included).
+ * workspace: device scratch of at least lat_attn_decode_workspace_size(...) bytes,
+ * 256-byte aligned; it must be zero-filled before its first use with a given layout
+ * (the kernel returns its merge counters to zero, so later calls need no reset), and
+ * calls sharing one workspace must not overlap on the GPU.  Too small ->
+ * LAT_ERR_WORKSPACE.  The size depends on the current device's SM count: size the
+ * workspace with the device current that will run the call.  LAT_F32 needs no
+ * workspace (its size is 0 and the pointer may be NULL).
+ * For LAT_BF16, q and the cache base pointers must be 16-byte aligned and q_rs,
+ * cache_rs, cache_head_stride, cache_seq_stride multiples of 8.
+ */
+lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
+                           const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,
+                           int64_t cache_seq_stride, const int32_t *kv_lens, int max_kv_len,
+                           void *out, int64_t out_rs, float *lse, int batch, int n_heads,
+                           int n_kv_heads, int head_dim, int window, float scale,
+                           void *workspace, size_t workspace_bytes, int32_t *status,
+                           void *stream);
+
+/*
+ * lat_kv_append — in-place KV-cache append: row pos[b] + t of sequence b's cache
+ * takes new row t, for t < n_new (the in-place "slice_set" append of the hf2q
+ * "Current Inference Path" page, sections 1 and 3, and the kv_cache_write step of
+ * the hf2q target page, section 6.1 step 6: "stride arithmetic must match exactly").
+ *
+ * Layout: caches as in lat_attn_decode; new element (b,t,hk,d) at
+ *   k_new[(b*n_new + t)*new_rs + hk*head_dim + d] (v_new likewise), so the new rows can
+ *   be column slices of a packed QKV buffer.  pos: device int32 [batch].
+ * A sequence whose rows would fall outside [0, capacity) is skipped whole and sets
+ * *status = LAT_ERR_BOUNDS.  New rows must not overlap the cache.
+ */
+lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
+                         int64_t cache_head_stride, int64_t cache_seq_stride, int capacity,
+                         const void *k_new, const void *v_new, int64_t new_rs,
+                         const int32_t *pos, int n_new, int batch, int n_kv_heads,
+                         int head_dim, int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAT_ATTN_H */

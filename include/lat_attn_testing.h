@@ -1,0 +1,31 @@
+/*
+ * lat_attn_testing.h — test hook of the lat_attn library.  Not part of the compute API.
+ *
+ * lat_test_prefill_timeout runs the bf16 prefill kernel (causal, kv_len = seq_len,
+ * scale 1/8, no lse) with its first K tile never loaded, so the tensor-core pipeline's
+ * bounded wait for that tile must run out after `timeout_ns` nanoseconds.  Each CTA then
+ * records LAT_ERR_TIMEOUT in *status (device int32, must be non-NULL and start at 0),
+ * drains its in-flight copies and MMAs, frees its tensor memory and exits, leaving the
+ * CUDA context usable.  Arguments and layout are those of lat_attn_prefill; the return
+ * value reports host-side validation and launch errors only.  The output is unspecified.
+ */
+#ifndef LAT_ATTN_TESTING_H
+#define LAT_ATTN_TESTING_H
+
+#include "lat_attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+lat_status lat_test_prefill_timeout(const void *q, int64_t q_rs, const void *k, int64_t k_rs,
+                                    const void *v, int64_t v_rs, void *out, int64_t out_rs,
+                                    int batch, int seq_len, int n_heads, int n_kv_heads,
+                                    int head_dim, uint64_t timeout_ns, int32_t *status,
+                                    void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAT_ATTN_TESTING_H */

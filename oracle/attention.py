@@ -115,13 +115,15 @@ class Oracle:
         kv_lens[b] - 1 (the prefill definition with S = 1, L = kv_lens[b]).
         Returns out [B, Hq, D], lse [B, Hq].
         """
-        q, k_cache, v_cache = _f64(q), _f64(k_cache), _f64(v_cache)
+        q = _f64(q)
         B, Hq, D = q.shape
         out = np.zeros((B, Hq, D), dtype=np.float64)
         lse = np.zeros((B, Hq), dtype=np.float64)
         for b in range(B):
             n = int(kv_lens[b])
-            o, l = self.prefill(q[b][None, None], k_cache[b, :n][None], v_cache[b, :n][None],
+            # only the visible prefix of each cache is converted (slots past n are unused)
+            kb, vb = _f64(k_cache[b, :n]), _f64(v_cache[b, :n])
+            o, l = self.prefill(q[b][None, None], kb[None], vb[None],
                                 causal=True, window=window, scale=scale, threads=threads)
             out[b], lse[b] = o[0, 0], l[0, 0]
         return out, lse

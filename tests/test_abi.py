@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared symbol, and
+rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from gqa_attention_lat_gb300 import binding
+from gqa_attention_lat_gb300.build import INCLUDE, build_library
+
+LAT_F32, LAT_BF16 = binding.LAT_F32, binding.LAT_BF16
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_library()
+    return binding.library(path)
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(INCLUDE, "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names.update(re.findall(r"\b(lat_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_headers_declare_the_three_calls():
+    names = declared_functions()
+    for n in ("lat_attn_prefill", "lat_attn_decode", "lat_kv_append",
+              "lat_attn_decode_workspace_size", "lat_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    assert set(declared_functions()) <= set(binding._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS_NAMES.items():
+        assert binding.lat_status_string(code) == name
+    assert binding.lat_status_string(99) == "LAT_ERR_UNKNOWN"
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
+
+
+def _prefill(**kw):
+    args = dict(dt=LAT_BF16, q=FAKE, q_rs=2048, k=FAKE, k_rs=2048, v=FAKE, v_rs=2048, out=FAKE,
+                out_rs=1024, lse=None, batch=1, seq_len=4, kv_len=4, n_heads=16, n_kv_heads=8,
+                head_dim=64, causal=1, window=0, scale=0.125)
+    args.update(kw)
+    return binding.lat_attn_prefill(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_heads=12, n_kv_heads=8), binding.LAT_ERR_INVALID_ARG),   # 12 % 8 != 0
+    (dict(head_dim=96, q_rs=4096, out_rs=4096), binding.LAT_ERR_UNSUPPORTED),
+    (dict(head_dim=32), binding.LAT_ERR_UNSUPPORTED),
+    (dict(kv_len=3), binding.LAT_ERR_INVALID_ARG),                   # kv_len < seq_len
+    (dict(batch=-1), binding.LAT_ERR_INVALID_ARG),
+    (dict(q=None), binding.LAT_ERR_INVALID_ARG),
+    (dict(q=FAKE + 2), binding.LAT_ERR_INVALID_ARG),                  # bf16 misaligned
+    (dict(k_rs=2044), binding.LAT_ERR_INVALID_ARG),                   # stride % 8
+    (dict(q_rs=512), binding.LAT_ERR_INVALID_ARG),                    # row narrower than heads
+    (dict(dt=7), binding.LAT_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.LAT_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_on_host(lib, kw, code):
+    with pytest.raises(binding.LatError) as e:
+        _prefill(**kw)
+    assert e.value.status == code
+
+
+def test_prefill_empty_is_a_no_op(lib):
+    _prefill(batch=0)
+    _prefill(seq_len=0, kv_len=0)
+
+
+def _decode(**kw):
+    args = dict(dt=LAT_BF16, q=FAKE, q_rs=4096, k_cache=FAKE, v_cache=FAKE, cache_rs=1024,
+                cache_head_stride=128, cache_seq_stride=4096 * 1024, kv_lens=FAKE,
+                max_kv_len=4096, out=FAKE, out_rs=4096, lse=None, batch=32, n_heads=32,
+                n_kv_heads=8, head_dim=128, window=0, scale=0.088, workspace=FAKE,
+                workspace_bytes=1 << 30)
+    args.update(kw)
+    return binding.lat_attn_decode(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_heads=30), binding.LAT_ERR_INVALID_ARG),
+    (dict(head_dim=100, q_rs=3200, out_rs=3200), binding.LAT_ERR_UNSUPPORTED),
+    (dict(kv_lens=None), binding.LAT_ERR_INVALID_ARG),
+    (dict(max_kv_len=-1), binding.LAT_ERR_INVALID_ARG),
+    (dict(cache_rs=0), binding.LAT_ERR_INVALID_ARG),
+    (dict(cache_rs=1020), binding.LAT_ERR_INVALID_ARG),               # bf16 stride % 8
+    (dict(k_cache=FAKE + 4), binding.LAT_ERR_INVALID_ARG),
+])
+def test_decode_rejects_on_host(lib, kw, code):
+    with pytest.raises(binding.LatError) as e:
+        _decode(**kw)
+    assert e.value.status == code
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    _decode(batch=0)
+
+
+def test_workspace_size_rejects_bad_shapes(lib):
+    assert binding.lat_attn_decode_workspace_size(LAT_F32, 8, 16, 8, 64, 100) == 0
+    assert binding.lat_attn_decode_workspace_size(LAT_BF16, 8, 15, 8, 64, 100) == 0
+    assert binding.lat_attn_decode_workspace_size(LAT_BF16, 8, 16, 8, 96, 100) == 0
+
+
+def _append(**kw):
+    args = dict(dt=LAT_BF16, k_cache=FAKE, v_cache=FAKE, cache_rs=1024, cache_head_stride=128,
+                cache_seq_stride=1024 * 64, capacity=64, k_new=FAKE, v_new=FAKE, new_rs=1024,
+                pos=FAKE, n_new=1, batch=2, n_kv_heads=8, head_dim=128)
+    args.update(kw)
+    return binding.lat_kv_append(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_kv_heads=0), binding.LAT_ERR_INVALID_ARG),
+    (dict(n_new=-1), binding.LAT_ERR_INVALID_ARG),
+    (dict(head_dim=48), binding.LAT_ERR_UNSUPPORTED),
+    (dict(pos=None), binding.LAT_ERR_INVALID_ARG),
+    (dict(new_rs=512), binding.LAT_ERR_INVALID_ARG),
+])
+def test_append_rejects_on_host(lib, kw, code):
+    with pytest.raises(binding.LatError) as e:
+        _append(**kw)
+    assert e.value.status == code
+
+
+def test_append_nothing_is_a_no_op(lib):
+    _append(n_new=0)
+    _append(batch=0)
+
+
+def test_library_is_sm103a_only():
+    from gqa_attention_lat_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
