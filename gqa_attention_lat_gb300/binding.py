@@ -41,6 +41,8 @@ _SIGNATURES = {
     "lat_attn_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lat_attn_decode": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _I64,
                                _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _P]),
+    "lat_attn_decode_static": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P,
+                                      _I64, _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P]),
     "lat_kv_append": (_I32, [_I32, _P, _P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _I32,
                              _I32, _I32, _I32, _P, _P]),
     "lat_test_prefill_timeout": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I32, _I32,
@@ -114,6 +116,18 @@ def lat_attn_decode(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
         cache_seq_stride, _ptr(kv_lens), max_kv_len, _ptr(out), out_rs, _ptr(lse), batch,
         n_heads, n_kv_heads, head_dim, window, scale, _ptr(workspace), workspace_bytes,
         _ptr(status), _stream(stream)), "lat_attn_decode")
+
+
+def lat_attn_decode_static(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                           cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch,
+                           n_heads, n_kv_heads, head_dim, window, scale, status=None,
+                           stream=None):
+    """lat_attn_decode with the library's own fixed device scratch (no workspace)."""
+    _check(library().lat_attn_decode_static(
+        dt, _ptr(q), q_rs, _ptr(k_cache), _ptr(v_cache), cache_rs, cache_head_stride,
+        cache_seq_stride, _ptr(kv_lens), max_kv_len, _ptr(out), out_rs, _ptr(lse), batch,
+        n_heads, n_kv_heads, head_dim, window, scale, _ptr(status), _stream(stream)),
+        "lat_attn_decode_static")
 
 
 def lat_kv_append(dt, k_cache, v_cache, cache_rs, cache_head_stride, cache_seq_stride,

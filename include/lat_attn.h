@@ -141,6 +141,35 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
                            void *stream);
 
 /*
+ * lat_attn_decode_static — lat_attn_decode without a caller workspace.  The pages have
+ * no counterpart to this call; it exists for callers that cannot allocate device
+ * memory: code running inside a host framework that owns all device memory, plugins
+ * whose host forbids allocation after start-up, and latency-critical paths that cannot
+ * afford an allocation's implicit synchronisation.
+ *
+ * Same arguments, layout and results as lat_attn_decode, minus workspace and
+ * workspace_bytes.  The split-KV scratch is one fixed 16 MiB array in device global
+ * memory that belongs to the library (every GPU the library is used on holds it until
+ * the process exits).  The call allocates nothing and calls no allocating routine.
+ * - Shapes whose scratch need (lat_attn_decode_workspace_size) exceeds 16 MiB return
+ *   LAT_ERR_WORKSPACE and launch nothing.
+ * - The first call on a device looks up the array's device address with that device
+ *   current and caches it; make that first call before any stream capture.
+ * - Every call on a device shares the array and it keeps the last call's contents: the
+ *   call clears the part that must start at zero (an asynchronous memset on `stream`
+ *   before the kernel), but calls that overlap on the GPU race on it, so serialise
+ *   them (one stream, or explicit events).
+ * - LAT_F32 needs no scratch and behaves exactly like lat_attn_decode.
+ */
+lat_status lat_attn_decode_static(lat_dtype dt, const void *q, int64_t q_rs,
+                                  const void *k_cache, const void *v_cache, int64_t cache_rs,
+                                  int64_t cache_head_stride, int64_t cache_seq_stride,
+                                  const int32_t *kv_lens, int max_kv_len, void *out,
+                                  int64_t out_rs, float *lse, int batch, int n_heads,
+                                  int n_kv_heads, int head_dim, int window, float scale,
+                                  int32_t *status, void *stream);
+
+/*
  * lat_kv_append — in-place KV-cache append: row pos[b] + t of sequence b's cache
  * takes new row t, for t < n_new (the in-place "slice_set" append of the hf2q
  * "Current Inference Path" page, sections 1 and 3, and the kv_cache_write step of

@@ -1,0 +1,61 @@
+"""lat_attn_decode_static: decode for callers that cannot allocate device memory.
+
+Callers inside a host framework that owns all device memory, or on a path where an
+allocation's implicit synchronisation is not acceptable, cannot hand lat_attn_decode a
+workspace.  This entry point keeps its split-KV scratch in a fixed array in the library's
+own device memory instead.  These checks call it through the C ABI and compare it with
+lat_attn_decode (which gets a freshly allocated workspace) on two calls in a row with
+different shapes, so the second call runs over whatever the first left in the shared
+array.  This file is collected last on purpose.
+"""
+import pytest
+import torch
+
+import workloads as W
+from gpu_helpers import DecodeRun, compare, ensure_library, status_tensor
+from gqa_attention_lat_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    ensure_library()
+
+
+def _decode_both(di, window, scale):
+    B, Hq, Hkv, D, cap = di.B, di.Hq, di.Hkv, di.D, di.cap
+    run = DecodeRun(di.dtype, B, Hq, Hkv, D, cap)
+    ref_out, ref_lse, st = run(di.q, di.k_cache, di.v_cache, Hkv * D, D, cap * Hkv * D,
+                               di.kv_lens, cap, B, Hq, Hkv, D, window, scale)
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    st2 = status_tensor()
+    binding.lat_attn_decode_static(binding.LAT_BF16 if di.dtype == "bf16" else binding.LAT_F32,
+                                   di.q, di.q.stride(0), di.k_cache, di.v_cache, Hkv * D, D,
+                                   cap * Hkv * D, di.kv_lens, cap, out, out.stride(0), lse, B, Hq,
+                                   Hkv, D, window, scale, st2)
+    torch.cuda.synchronize()
+    assert st.item() == 0 and st2.item() == 0
+    return out, lse, ref_out, ref_lse
+
+
+def test_static_scratch_decode_matches_workspace_decode_twice():
+    first = W.decode_inputs(4, 16, 2, 128, 3000, kv_lens=[3000, 1500, 17, 1], device="cuda",
+                            seed=W.BASE_SEED + 11)
+    second = W.decode_inputs(3, 8, 2, 64, 1000, kv_lens=[1000, 999, 500], device="cuda",
+                             seed=W.BASE_SEED + 12)
+    for di, window in ((first, 0), (second, 100)):
+        out, lse, ref_out, ref_lse = _decode_both(di, window, 1.0 / di.D ** 0.5)
+        compare(out.view(di.B, di.Hq, di.D),
+                ref_out.view(di.B, di.Hq, di.D).double().cpu().numpy(), di.dtype,
+                "static scratch vs workspace", lse, ref_lse.double().cpu().numpy())
+
+
+def test_static_scratch_rejects_shapes_beyond_its_maximum():
+    fake = 0x10000  # never dereferenced: the size check comes first
+    with pytest.raises(binding.LatError) as e:
+        binding.lat_attn_decode_static(binding.LAT_BF16, fake, 16 * 512, fake, fake, 2 * 512,
+                                       512, 32768 * 2 * 512, fake, 32768, fake, 16 * 512, None,
+                                       1024, 16, 2, 512, 0, 0.04)
+    assert e.value.status == binding.LAT_ERR_WORKSPACE
