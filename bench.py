@@ -229,10 +229,14 @@ class DecodeStep:
         self.lse = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
-    def __call__(self):
+    def __call__(self, q=None, k_cache=None, v_cache=None, kv_lens=None):
         d, wl = self.di, self.wl
-        self.b.lat_attn_decode(self.dt, d.q, d.q.stride(0), d.k_cache, d.v_cache, wl.Hkv * wl.D,
-                               wl.D, wl.L * wl.Hkv * wl.D, d.kv_lens, wl.L, self.out,
+        q = d.q if q is None else q
+        k_cache = d.k_cache if k_cache is None else k_cache
+        v_cache = d.v_cache if v_cache is None else v_cache
+        kv_lens = d.kv_lens if kv_lens is None else kv_lens
+        self.b.lat_attn_decode(self.dt, q, d.q.stride(0), k_cache, v_cache, wl.Hkv * wl.D,
+                               wl.D, wl.L * wl.Hkv * wl.D, kv_lens, wl.L, self.out,
                                self.out.stride(0), self.lse, wl.B, wl.Hq, wl.Hkv, wl.D,
                                wl.window, wl.scale, self.ws, self.nbytes, self.status)
 
@@ -279,24 +283,40 @@ def measure_extra(device, flush, stream, peaks, reps=10):
 
 
 def e2e_measure(step, steps, stream):
-    """Host buffers through the C ABI: upload QKV from pinned memory, run, download."""
-    wl, inp = step.wl, step.inp
-    parent = inp.packed if inp.packed is not None else None
-    if parent is None:
-        raise RuntimeError("e2e leg expects the packed QKV workload")
-    host_in = torch.empty(parent.shape, dtype=parent.dtype, pin_memory=True)
-    host_in.copy_(parent.cpu())
-    host_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype, pin_memory=True)
-    dev_in = torch.empty_like(parent)
-    qw, kw = wl.Hq * wl.D, wl.Hkv * wl.D
-    q, k, v = dev_in[:, :qw], dev_in[:, qw:qw + kw], dev_in[:, qw + kw:]
+    """Host buffers through the C ABI: upload the step's inputs from pinned memory, run,
+    download the outputs (and lse).  Returns (ms per step, h2d bytes, d2h bytes)."""
+    if isinstance(step, PrefillStep):
+        wl, inp = step.wl, step.inp
+        if inp.packed is not None:
+            parents = [inp.packed]
+        else:
+            parents = [inp.q.contiguous(), inp.k.contiguous(), inp.v.contiguous()]
+        outs = [step.out, step.lse]
+    else:
+        d = step.di
+        parents = [d.q, d.k_cache, d.v_cache, d.kv_lens]
+        outs = [step.out, step.lse]
+    hosts = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in parents]
+    for h, p in zip(hosts, parents):
+        h.copy_(p.cpu())
+    devs = [torch.empty_like(p) for p in parents]
+    host_outs = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    if isinstance(step, PrefillStep):
+        if inp.packed is not None:
+            qw, kw = wl.Hq * wl.D, wl.Hkv * wl.D
+            buf = devs[0]
+            args = (buf[:, :qw], buf[:, qw:qw + kw], buf[:, qw + kw:])
+        else:
+            args = tuple(devs)
+    else:
+        args = tuple(devs)
 
     def one():
-        dev_in.copy_(host_in, non_blocking=True)
-        step(q, k, v)
-        host_out.copy_(step.out, non_blocking=True)
-        host_lse.copy_(step.lse, non_blocking=True)
+        for dv, h in zip(devs, hosts):
+            dv.copy_(h, non_blocking=True)
+        step(*args)
+        for h, o in zip(host_outs, outs):
+            h.copy_(o, non_blocking=True)
 
     for _ in range(3):
         one()
@@ -308,8 +328,8 @@ def e2e_measure(step, steps, stream):
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
-    h2d = host_in.numel() * host_in.element_size()
-    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    d2h = sum(h.numel() * h.element_size() for h in host_outs)
     return ms, h2d, d2h
 
 
@@ -378,6 +398,13 @@ def run_reference(args, rank, world):
 
 
 def workload_config(wl):
+    if wl.kind == "decode":
+        return {"workload": "%s: decode B%d Hq%d Hkv%d D%d cache %d, kv_len %s %s" % (
+            wl.name, wl.B, wl.Hq, wl.Hkv, wl.D, wl.L,
+            "uniform[1,%d]" % wl.L if wl.kv_lens is None else str(wl.kv_lens), wl.dtype),
+            "batch": wl.B, "kv_capacity": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
+            "head_dim": wl.D, "window": wl.window,
+            "l2": "flushed before every timed step (256 MiB write)", "parallelism": "replicas"}
     return {"workload": "%s: B%d S%d Hq%d Hkv%d D%d %s%s %s%s" % (
         wl.name, wl.B, wl.S, wl.Hq, wl.Hkv, wl.D, "causal" if wl.causal else "full",
         " window %d" % wl.window if wl.window else "", wl.dtype,
@@ -431,10 +458,10 @@ def main():
     stream = torch.cuda.current_stream(device)
     peaks, peak_src = load_peaks()
     wl = W.WORKLOADS[args.workload]
-    if wl.kind != "prefill" or wl.dtype != "bf16":
-        raise SystemExit("the headline workload must be a bf16 prefill")
+    if wl.dtype != "bf16":
+        raise SystemExit("bench workloads are bf16 (the fp32 shapes are parity cases)")
     flush = Flusher(device)
-    step = PrefillStep(wl, device)
+    step = PrefillStep(wl, device) if wl.kind == "prefill" else DecodeStep(wl, device)
     sampler = ClockSampler(local)
     sampler.start()
     for _ in range(args.warmup):
@@ -457,15 +484,28 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
     ms_per_step = ms_total / args.steps
-    flops, alg_bytes, pairs = prefill_work(wl)
-    value = flops * world / (ms_per_step / 1e3) / 1e12
+    if wl.kind == "prefill":
+        flops, alg_bytes, _ = prefill_work(wl)
+        unit, work = "TFLOP/s", flops / 1e12
+        kernel = "prefill_tc_kernel<%d>" % wl.D
+        intensity = flops / alg_bytes
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        bound = "hbm" if intensity < ridge else "tensor"
+        profile, srcs = "prefill_tc_%s.md" % wl.name, ["prefill_tc.cu", "device_common.cuh", "kernels.h"]
+    else:
+        flops, alg_bytes, _ = decode_work(wl, step.di.kv_lens.cpu().tolist())
+        unit, work = "GB/s", alg_bytes / 1e9
+        kernel = "decode_bf16_kernel<%d>" % wl.D
+        bound = "hbm"
+        profile, srcs = "decode_bf16_%s.md" % wl.name, ["decode_bf16.cu", "device_common.cuh", "kernels.h"]
+    value = work * world / (ms_per_step / 1e3)
 
     e2e_ms, h2d, d2h = e2e_measure(step, args.steps, stream)
     if dist is not None:
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    e2e_value = flops * world / (e2e_ms / 1e3) / 1e12
+    e2e_value = work * world / (e2e_ms / 1e3)
 
     extra = None
     if not args.no_extra:
@@ -475,26 +515,28 @@ def main():
     clocks = sampler.stop()
 
     cpu = None
-    if not args.no_cpu and rank == 0 and world == 1:
+    if not args.no_cpu and rank == 0 and world == 1 and wl.kind == "prefill":
         cpu = cpu_baseline(wl)
 
     kernel_ms = statistics.mean(ms_steps)
-    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
-    traffic = profile_traffic("prefill_tc_qwen3_0.6b_prefill.md",
-                              ["prefill_tc.cu", "device_common.cuh", "kernels.h"])
+    if bound == "hbm":
+        achieved, peak, r_unit = alg_bytes / (kernel_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, r_unit = flops / (kernel_ms / 1e3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    traffic = profile_traffic(profile, srcs)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16-rounded)",
         "config": workload_config(wl),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "prefill_tc_kernel<64>", "peak_source": peak_src,
-                     "algorithmic_bytes": alg_bytes,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": r_unit,
+                     "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
+                     "peak_source": peak_src, "algorithmic_bytes": alg_bytes,
+                     "algorithmic_flops": flops,
                      "tensor_frac": (flops / (kernel_ms / 1e3) / 1e12) / peaks["bf16_tflops"]},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps,
         "clocks": clocks,

@@ -13,10 +13,14 @@
 //    loads, warp 5 issues tcgen05.mma.  Synchronisation is by mbarriers only.
 //  * S = Q K^T is accumulated in tensor memory (fp32, double-buffered so the MMA of tile
 //    j+1 overlaps the softmax of tile j); P = exp2(S*scale*log2e - m) is written as bf16
-//    to shared memory and O += P V accumulates in tensor memory.
-//  * K and V reach shared memory as [BN keys x 64 head-dims] chunks with 128-byte
-//    swizzle, through one ring of chunk slots that the MMA warp consumes in issue order.
-//    Q and K enter the MMA K-major; V enters MN-major, one 64-column chunk per MMA.
+//    back into the S buffer it came from, and O += P V reads it straight from tensor
+//    memory (one MMA per 16 keys covering all of this CTA's O columns).
+//  * K and V tiles reach shared memory through two rings (one for K tiles, one for V
+//    tiles), each tile a set of [BN keys x 64 head-dims] chunks with 128-byte swizzle
+//    filled by its own producer warp under ONE mbarrier per tile: a TMA producer that
+//    arms a barrier per small chunk spends most of its time on the barrier round trip,
+//    and the consumer would wait once per chunk.  Q and K enter the MMA K-major; V
+//    enters MN-major, one 64-column chunk per MMA.
 //  * Tiles wholly outside the causal / window band are never loaded or computed; tiles
 //    wholly inside it skip the per-element mask.
 //  * The running maximum is refreshed only when it grows by more than 2^8 (the stale
@@ -38,9 +42,11 @@ namespace lat {
 namespace {
 
 constexpr int kBM = 128;             // query rows per CTA (= TMEM lanes)
-constexpr int kThreads = 192;        // 4 softmax warps + producer warp + MMA warp
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 352;        // 8 softmax warps + K and V producer warps + MMA warp
+constexpr int kSoftmaxThreads = 256;
+constexpr int kKProducerWarp = 8;
+constexpr int kVProducerWarp = 9;
+constexpr int kMmaWarp = 10;
 constexpr int kChunkCols = 64;       // head-dim columns per swizzled chunk (128 bytes)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;       // O accumulator columns [0, 256)
@@ -51,20 +57,27 @@ template <int D>
 struct TcCfg {
     static constexpr int kQkChunks = (D + kChunkCols - 1) / kChunkCols;   // Q/K chunks
     static constexpr int kKSteps = (D + 15) / 16;                          // S MMA k-steps
-    static constexpr int kBN = D <= 128 ? 128 : 64;                        // keys per tile
+    static constexpr int kBN = D <= 256 ? 128 : 64;                        // keys per tile
     static constexpr int kSplitO = D == 512 ? 2 : 1;                       // CTAs per O row
     static constexpr int kOCols = D / kSplitO;                             // O cols per CTA
     static constexpr int kVChunks = (kOCols + kChunkCols - 1) / kChunkCols;
-    static constexpr int kSlotBytes = kBN * 128;
+    static constexpr int kChunkBytes = kBN * 128;                          // one [BN x 64] chunk
+    static constexpr int kKTileBytes = kQkChunks * kChunkBytes;
+    static constexpr int kVTileBytes = kVChunks * kChunkBytes;
+    static constexpr int kKStages = D == 64 ? 4 : (D <= 128 ? 3 : 1);
+    static constexpr int kVStages = D == 64 ? 4 : (D <= 128 ? 2 : 1);
     static constexpr int kQBytes = kQkChunks * kBM * 128;
-    static constexpr int kPChunks = kBN / 64;
-    static constexpr int kPBytes = kPChunks * kBM * 128;
-    static constexpr int kSlots = D == 512 ? 10 : (D == 256 ? 16 : 8);
-    static constexpr int kBarBytes = 1024;
-    static constexpr int kSmem = 1024 /*align slack*/ + kQBytes + kPBytes +
-                                 kSlots * kSlotBytes + kBarBytes;
+    static constexpr int kBarBytes = 256 + 4 * kBM * 4;  // barriers + row exchange
+    static constexpr int kPayload = kQBytes + kKStages * kKTileBytes + kVStages * kVTileBytes +
+                                    kBarBytes;
+    // 1 KB of slack lets the 1024-byte aligned carve-up start anywhere; a shape that
+    // cannot afford it relies on the dynamic shared memory base being 1024-byte aligned
+    // (checked at run time)
+    static constexpr int kSlack = kPayload + 1024 <= 232448 ? 1024 : 0;
+    static constexpr int kSmem = kSlack + kPayload;
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(kOCols <= 256 && kTmemS + 2 * kBN <= kTmemCols, "tensor memory budget");
+    static_assert(kBN % 32 == 0, "P columns per warpgroup must fill whole TMEM stores");
 };
 
 // ---- tcgen05 descriptors ----------------------------------------------------------
@@ -79,6 +92,19 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
     d |= (uint64_t)(1024 >> 4) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// The same for an MN-major operand whose 64-column atoms sit `atom_stride` bytes apart:
+// the leading byte offset is the stride between atoms along N, the stride byte offset
+// the 1024 bytes between 8-row groups along K.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t atom_stride) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)(atom_stride >> 4) << 16;
     d |= (uint64_t)(1024 >> 4) << 32;
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
@@ -114,22 +140,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     using C = TcCfg<D>;
     constexpr int BN = C::kBN;
-    extern __shared__ unsigned char smem_raw[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (C::kSlack == 0 && smem != smem_raw) {  // no room to realign: refuse to run
+        if (threadIdx.x == 0) report_status(a.status, kErrCuda);
+        return;
+    }
     unsigned char *sQ = smem;
-    unsigned char *sP = sQ + C::kQBytes;
-    unsigned char *sSlots = sP + C::kPBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sSlots + C::kSlots * C::kSlotBytes);
+    unsigned char *sK = sQ + C::kQBytes;                      // [kKStages] K tiles
+    unsigned char *sV = sK + C::kKStages * C::kKTileBytes;    // [kVStages] V tiles
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sV + C::kVStages * C::kVTileBytes);
     uint64_t *bar_q = bars + 0;
     uint64_t *bar_s = bars + 1;        // [2]
-    uint64_t *bar_p = bars + 3;
-    uint64_t *bar_o = bars + 4;
-    uint64_t *bar_done = bars + 5;     // final MMA drain
-    uint64_t *bar_full = bars + 6;     // [kSlots]
-    uint64_t *bar_empty = bar_full + C::kSlots;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_empty + C::kSlots);
+    uint64_t *bar_p = bars + 3;        // [2] P(t) ready, alternating by tile parity
+    uint64_t *bar_o = bars + 5;
+    uint64_t *bar_done = bars + 6;     // every MMA complete (drain and epilogue)
+    uint64_t *bar_x = bars + 7;        // [4] softmax row exchange, one per TMEM lane quarter
+    uint64_t *k_full = bars + 11;      // [kKStages]
+    uint64_t *k_empty = k_full + C::kKStages;
+    uint64_t *v_full = k_empty + C::kKStages;   // [kVStages]
+    uint64_t *v_empty = v_full + C::kVStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(v_empty + C::kVStages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *xchg = reinterpret_cast<float *>(bars + 32);   // [2 parities][2 warpgroups][kBM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int head_sel = blockIdx.x;               // h * kSplitO + half
@@ -150,12 +184,18 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         mbar_init(bar_q, 1);
         mbar_init(&bar_s[0], 1);
         mbar_init(&bar_s[1], 1);
-        mbar_init(bar_p, 128);
+        mbar_init(&bar_p[0], kSoftmaxThreads);
+        mbar_init(&bar_p[1], kSoftmaxThreads);
+        for (int q = 0; q < 4; ++q) mbar_init(&bar_x[q], 2);  // one arrival per warp
         mbar_init(bar_o, 1);
         mbar_init(bar_done, 1);
-        for (int s = 0; s < C::kSlots; ++s) {
-            mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -169,55 +209,47 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == kKProducerWarp || warp == kVProducerWarp) {
+        // ------------------------------------------------------------ TMA producers
+        // warp 8 loads Q, then every K tile; warp 9 loads every V tile (this CTA's O
+        // columns).  One mbarrier per tile carries all of the tile's chunk copies.
         if (lane == 0) {
-            tma_prefetch_desc(&a.tm_q);
-            tma_prefetch_desc(&a.tm_k);
-            tma_prefetch_desc(&a.tm_v);
-            mbar_arrive_expect_tx(bar_q, C::kQBytes);
-            for (int c = 0; c < C::kQkChunks; ++c)
-                tma_load_4d(sQ + c * kBM * 128, &a.tm_q, bar_q, c * kChunkCols, h, m0, b);
-            int issued[C::kSlots];
-            for (int s = 0; s < C::kSlots; ++s) issued[s] = 0;
-            int r = 0;
-            bool ok = true;
-            auto push = [&](const CUtensorMap *tm, int col, int key0) {
-                const int s = r % C::kSlots;
-                if (!mbar_wait_bounded(&bar_empty[s], ((r / C::kSlots) & 1) ^ 1, abort_flag,
-                                       deadline)) {
-                    ok = false;
-                    return;
-                }
-                mbar_arrive_expect_tx(&bar_full[s], C::kSlotBytes);
-                tma_load_4d(sSlots + s * C::kSlotBytes, tm, &bar_full[s], col, hk, key0, b);
-                ++issued[s];
-                ++r;
-            };
-            for (int t = 0; t <= n_tiles && ok; ++t) {
-                if (t < n_tiles) {
-                    const int key0 = (band.t_begin + t) * BN;
-                    for (int c = 0; c < C::kQkChunks && ok; ++c) {
-                        if (a.test_skip_kv_load && t == 0 && c == 0) {  // test hook
-                            ++r;
-                            continue;
-                        }
-                        push(&a.tm_k, c * kChunkCols, key0);
-                    }
-                }
-                if (t > 0) {
-                    const int key0 = (band.t_begin + t - 1) * BN;
-                    for (int c = 0; c < C::kVChunks && ok; ++c)
-                        push(&a.tm_v, v_col0 + c * kChunkCols, key0);
-                }
+            const bool is_k = warp == kKProducerWarp;
+            const int stages = is_k ? C::kKStages : C::kVStages;
+            const int tile_bytes = is_k ? C::kKTileBytes : C::kVTileBytes;
+            const int chunks = is_k ? C::kQkChunks : C::kVChunks;
+            unsigned char *ring = is_k ? sK : sV;
+            uint64_t *full = is_k ? k_full : v_full;
+            uint64_t *empty = is_k ? k_empty : v_empty;
+            const CUtensorMap *tm = is_k ? &a.tm_k : &a.tm_v;
+            const int col0 = is_k ? 0 : v_col0;
+            tma_prefetch_desc(tm);
+            if (is_k) {
+                tma_prefetch_desc(&a.tm_q);
+                mbar_arrive_expect_tx(bar_q, C::kQBytes);
+                for (int c = 0; c < C::kQkChunks; ++c)
+                    tma_load_4d(sQ + c * kBM * 128, &a.tm_q, bar_q, c * kChunkCols, h, m0, b);
+            }
+            int last_issued[4] = {-1, -1, -1, -1};  // per stage: tile index of its last load
+            for (int t = 0; t < n_tiles; ++t) {
+                const int s = t % stages;
+                if (!mbar_wait_bounded(&empty[s], ((t / stages) & 1) ^ 1, abort_flag, deadline))
+                    break;
+                if (is_k && a.test_skip_kv_load && t == 0) continue;  // test hook: never load
+                mbar_arrive_expect_tx(&full[s], tile_bytes);
+                const int key0 = (band.t_begin + t) * BN;
+                for (int c = 0; c < chunks; ++c)
+                    tma_load_4d(ring + s * tile_bytes + c * C::kChunkBytes, tm, &full[s],
+                                col0 + c * kChunkCols, hk, key0, b);
+                last_issued[s] = t;
             }
             // drain: every issued copy must land before the CTA may exit
             const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
             volatile int no_abort = 0;
-            mbar_wait_bounded(bar_q, 0, &no_abort, drain_deadline);
-            for (int s = 0; s < C::kSlots; ++s)
-                if (issued[s] > 0)
-                    mbar_wait_bounded(&bar_full[s], (issued[s] - 1) & 1, &no_abort,
+            if (is_k) mbar_wait_bounded(bar_q, 0, &no_abort, drain_deadline);
+            for (int s = 0; s < stages; ++s)
+                if (last_issued[s] >= 0)
+                    mbar_wait_bounded(&full[s], (last_issued[s] / stages) & 1, &no_abort,
                                       drain_deadline);
         }
         __syncwarp();
@@ -225,65 +257,58 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = instr_desc(kBM, BN, false);
-            const uint32_t q_base = smem_u32(sQ);
-            const uint32_t p_base = smem_u32(sP);
-            const uint32_t slot_base = smem_u32(sSlots);
+            // Descriptors are built once; advancing an operand by B bytes adds B >> 4 to
+            // the start-address field (all smem addresses here are below 256 KB, so the
+            // 14-bit field never carries), which keeps the issue loop to a few
+            // instructions per MMA.
+            const uint64_t dq0 = sw128_desc(smem_u32(sQ));
+            const uint64_t dk0 = sw128_desc(smem_u32(sK));
             bool ok = mbar_wait_bounded(bar_q, 0, abort_flag, deadline);
-            int r = 0;
             tc_fence_after();
-            auto take = [&](int &s) {
-                s = r % C::kSlots;
-                if (!mbar_wait_bounded(&bar_full[s], (r / C::kSlots) & 1, abort_flag, deadline))
-                    return false;
-                tc_fence_after();
-                return true;
-            };
             for (int t = 0; t <= n_tiles && ok; ++t) {
                 if (t < n_tiles) {
                     // S(t) = Q K(t)^T into S buffer t % 2
+                    const int s = t % C::kKStages;
+                    if (!mbar_wait_bounded(&k_full[s], (t / C::kKStages) & 1, abort_flag, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     const uint32_t d_s = tmem + kTmemS + (uint32_t)((t & 1) * BN);
-                    for (int c = 0; c < C::kQkChunks && ok; ++c) {
-                        int s;
-                        if (!take(s)) { ok = false; break; }
-                        const uint32_t k_addr = slot_base + s * C::kSlotBytes;
-                        const uint32_t q_addr = q_base + c * kBM * 128;
+                    const uint64_t dk = dk0 + (uint64_t)((s * C::kKTileBytes) >> 4);
+#pragma unroll
+                    for (int c = 0; c < C::kQkChunks; ++c) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
                             if (c * 4 + kk < C::kKSteps)
-                                tc_mma_ss(d_s, sw128_desc(q_addr + kk * 32),
-                                          sw128_desc(k_addr + kk * 32), idesc_s,
-                                          (c > 0 || kk > 0) ? 1u : 0u);
+                                tc_mma_ss(d_s, dq0 + (uint64_t)((c * kBM * 128 + kk * 32) >> 4),
+                                          dk + (uint64_t)((c * C::kChunkBytes + kk * 32) >> 4),
+                                          idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc_commit(&bar_empty[s]);
-                        ++r;
                     }
-                    if (!ok) break;
+                    tc_commit(&k_empty[s]);
                     tc_commit(&bar_s[t & 1]);
                 }
                 if (t > 0) {
-                    // O += P(t-1) V(t-1), one 64-column chunk of V at a time
+                    // O += P(t-1) V(t-1): A = P from tensor memory (the S buffer it was
+                    // computed from, 8 columns per 16 keys), B = V MN-major with its 64-column
+                    // atoms kChunkBytes apart, N = every O column of this CTA
                     const int tp = t - 1;
-                    if (!mbar_wait_bounded(bar_p, tp & 1, abort_flag, deadline)) { ok = false; break; }
-                    tc_fence_after();
-                    for (int c = 0; c < C::kVChunks && ok; ++c) {
-                        int s;
-                        if (!take(s)) { ok = false; break; }
-                        const uint32_t v_addr = slot_base + s * C::kSlotBytes;
-                        const int ncols = min(kChunkCols, C::kOCols - c * kChunkCols);
-                        const uint32_t idesc_pv = instr_desc(kBM, ncols, true);
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            // A = P, K-major: keys 16kk..16kk+15 live in chunk kk/4 at +32B*(kk%4)
-                            const uint32_t a_addr = p_base + (kk >> 2) * kBM * 128 + (kk & 3) * 32;
-                            // B = V, MN-major: 16 keys = two 8-row groups = 2048 bytes
-                            const uint32_t b_addr = v_addr + kk * 2048;
-                            tc_mma_ss(tmem + kTmemO + c * kChunkCols, sw128_desc(a_addr),
-                                      sw128_desc(b_addr), idesc_pv, (tp > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc_commit(&bar_empty[s]);
-                        ++r;
+                    const int s = tp % C::kVStages;
+                    if (!mbar_wait_bounded(&bar_p[tp & 1], (tp >> 1) & 1, abort_flag, deadline) ||
+                        !mbar_wait_bounded(&v_full[s], (tp / C::kVStages) & 1, abort_flag, deadline)) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dv = sw128_desc_mn(smem_u32(sV) + s * C::kVTileBytes, C::kChunkBytes);
+                    const uint32_t p_tmem = tmem + kTmemS + (uint32_t)((tp & 1) * BN);
+                    constexpr uint32_t idesc_pv = instr_desc(kBM, C::kOCols, true);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc_mma_ts(tmem + kTmemO, p_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
+                                  idesc_pv, (tp > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&v_empty[s]);
                     tc_commit(bar_o);
                 }
             }
@@ -295,107 +320,147 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps
-        const int row = threadIdx.x;                  // 0..127, TMEM lane
+        // Two warpgroups share every row: warp w and warp w+4 read the same TMEM lane
+        // quarter; warpgroup g owns S columns [g*BN/2, (g+1)*BN/2) of each tile and O
+        // column chunks k (16 wide) with k % 2 == g.  Their partial row maxima meet in
+        // shared memory once per tile (an mbarrier per lane quarter, double-buffered).
+        constexpr int HC = BN / 2;                    // S columns per thread
+        const int wg = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
         const int i = m0 + row;                       // query row within the sequence
         const int p = i + (a.kv_len - a.seq_len);     // its absolute position
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int col0 = wg * HC;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float sl2 = a.scale_log2;
+        const bool max_mode = sl2 >= 0.f;             // a negative scale flips max and min
+        const float hide = max_mode ? -INFINITY : INFINITY;  // raw value that never wins
         float m_ref = -INFINITY;  // reference maximum (log2 domain, scaled)
-        float l_sum = 0.f;
+        float l_part = 0.f;       // this warpgroup's share of the row sum
         bool ok = true;
         // tcgen05.ld/st are warp-collective, so a wait's outcome is made warp-uniform
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
             const bool r = mbar_wait_bounded(bar, parity, abort_flag, deadline);
             return __all_sync(0xffffffffu, r) != 0;
         };
+        // publish v for the partner warp and read the partner's value (use n of the
+        // exchange barrier of this lane quarter)
+        auto exchange = [&](float v, int n, float &other) {
+            xchg[((n & 1) * 2 + wg) * kBM + row] = v;
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_x[quarter]);
+            if (!wait_warp(&bar_x[quarter], n & 1)) return false;
+            other = xchg[((n & 1) * 2 + (wg ^ 1)) * kBM + row];
+            return true;
+        };
         for (int t = 0; t < n_tiles; ++t) {
             if (!wait_warp(&bar_s[t & 1], (t >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
-            float sv[BN];
+            float sv[HC];
 #pragma unroll
-            for (int c = 0; c < BN; c += 16)
-                tmem_ld16(lane_base + kTmemS + (t & 1) * BN + c, reinterpret_cast<uint32_t *>(sv + c));
+            for (int c = 0; c < HC; c += 16)
+                tmem_ld16(lane_base + kTmemS + (t & 1) * BN + col0 + c,
+                          reinterpret_cast<uint32_t *>(sv + c));
             tc_wait_ld();
 
             const int key0 = (band.t_begin + t) * BN;
-            const bool need_mask = (key0 + BN > a.kv_len) ||
-                                   (a.causal && key0 + BN - 1 > m0 + (a.kv_len - a.seq_len)) ||
-                                   (a.window > 0 && key0 < m0 + rows - 1 + (a.kv_len - a.seq_len) - a.window + 1);
-            float mx = -INFINITY;
+            const int p_min = m0 + (a.kv_len - a.seq_len);
+            const bool need_mask = (key0 + BN > a.kv_len) || (a.causal && key0 + BN - 1 > p_min) ||
+                                   (a.window > 0 && key0 < p_min + rows - 1 - a.window + 1);
+            // visible columns of this thread's half: [vlo, vhi)
+            int vlo = 0, vhi = HC;
             if (need_mask) {
+                const int kc0 = key0 + col0;
+                int jhi = a.kv_len;
+                if (a.causal) jhi = min(jhi, p + 1);
+                vhi = max(0, min(HC, jhi - kc0));
+                if (a.window > 0) vlo = min(HC, max(0, p - a.window + 1 - kc0));
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const int j = key0 + c;
-                    const bool vis = j < a.kv_len && (!a.causal || j <= p) &&
-                                     (a.window <= 0 || p - j < a.window);
-                    sv[c] = vis ? sv[c] * a.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
-                }
+                for (int c = 0; c < HC; ++c)
+                    if (c < vlo || c >= vhi) sv[c] = hide;
+            }
+            float e[4] = {hide, hide, hide, hide};
+            if (max_mode) {
+#pragma unroll
+                for (int c = 0; c < HC; ++c) e[c & 3] = fmaxf(e[c & 3], sv[c]);
             } else {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    sv[c] *= a.scale_log2;
-                    mx = fmaxf(mx, sv[c]);
-                }
+                for (int c = 0; c < HC; ++c) e[c & 3] = fminf(e[c & 3], sv[c]);
             }
+            const float ext = max_mode ? fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]))
+                                       : fminf(fminf(e[0], e[1]), fminf(e[2], e[3]));
+            const float mx_part = vhi > vlo ? ext * sl2 : -INFINITY;
+            float mx_other;
+            if (!exchange(mx_part, t, mx_other)) { ok = false; break; }
+            const float mx = fmaxf(mx_part, mx_other);
+
             // refresh the reference maximum only when it grew by more than the threshold
             const bool refresh = mx > m_ref + kRescaleThreshold;
             const float m_new = refresh ? mx : m_ref;
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            float rowsum = 0.f;
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;  // no key seen yet
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
+            if (need_mask) {
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                sv[c] = fast_exp2(sv[c] - m_use);
-                rowsum += sv[c];
+                for (int c = 0; c < HC; ++c) {
+                    const float w = fast_exp2(fmaf(sv[c], sl2, -m_use));
+                    sv[c] = (c >= vlo && c < vhi) ? w : 0.f;
+                    rs[c & 3] += sv[c];
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < HC; ++c) {
+                    sv[c] = fast_exp2(fmaf(sv[c], sl2, -m_use));
+                    rs[c & 3] += sv[c];
+                }
             }
             const float corr = refresh ? fast_exp2(m_ref - m_use) : 1.f;  // 0 when m_ref = -inf
 
-            // P and O are free once P(t-1) V(t-1) has completed
-            if (t > 0) {
-                if (!wait_warp(bar_o, (t - 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-            }
-            // P (bf16) into shared memory, K-major with 128-byte swizzle: row `row`,
-            // keys 8u..8u+7 of chunk c at 16-byte unit u ^ (row & 7)
+            // this half of P (bf16 pairs) into the S buffer it came from: both warpgroups
+            // have read their S columns (the exchange above orders that), and P(t) sits
+            // where PV(t) will read it
+            {
+                const uint32_t pcol = lane_base + kTmemS + (t & 1) * BN + col0 / 2;
 #pragma unroll
-            for (int c = 0; c < C::kPChunks; ++c) {
-                unsigned char *prow = sP + c * kBM * 128 + row * 128;
+                for (int c = 0; c < HC / 2; c += 8) {
+                    uint32_t pk[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float *x = sv + c * 64 + u * 8;
-                    uint4 pk;
-                    pk.x = pack_bf16x2(x[0], x[1]);
-                    pk.y = pack_bf16x2(x[2], x[3]);
-                    pk.z = pack_bf16x2(x[4], x[5]);
-                    pk.w = pack_bf16x2(x[6], x[7]);
-                    *reinterpret_cast<uint4 *>(prow + ((u ^ (row & 7)) << 4)) = pk;
+                    for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(sv[2 * (c + k)], sv[2 * (c + k) + 1]);
+                    tmem_st8(pcol + c, pk);
                 }
             }
-            // rescale O in tensor memory when any row of this warp refreshed its maximum
+            // rescale this warpgroup's O chunks when any row of the warp refreshed; O is
+            // stable once PV(t-1) completes (the S(t) commit already covered PV(t-2), so
+            // phase t-1 of bar_o is the next one to complete)
             if (t > 0 && __any_sync(0xffffffffu, refresh)) {
+                if (!wait_warp(bar_o, (t - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < C::kOCols; c += 16) {
+                for (int c = 16 * wg; c < C::kOCols; c += 32) {
                     uint32_t ov[16];
                     tmem_ld16(lane_base + kTmemO + c, ov);
                     tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+                    for (int k = 0; k < 16; ++k)
+                        ov[k] = __float_as_uint(__uint_as_float(ov[k]) * corr);
                     tmem_st16(lane_base + kTmemO + c, ov);
                 }
-                tc_wait_st();
             }
-            l_sum = l_sum * corr + rowsum;
+            tc_wait_st();
+            l_part = l_part * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
             m_ref = m_new;
-            fence_proxy_async_smem();  // P writes -> visible to the tensor core
             tc_fence_before();
-            mbar_arrive(bar_p);
+            mbar_arrive(&bar_p[t & 1]);
         }
         // ---- epilogue: O / l -> bf16 rows, lse -----------------------------------
         if (ok && n_tiles > 0) {
-            ok = wait_warp(bar_o, (n_tiles - 1) & 1);
+            ok = wait_warp(bar_done, 0);
             tc_fence_after();
         }
+        float l_other = 0.f;
+        if (ok) ok = exchange(l_part, n_tiles, l_other);
         if (ok) {
+            const float l_sum = l_part + l_other;
             const bool live = row < rows;  // rows past the sequence end are not stored
             const int64_t qrow = (int64_t)b * a.seq_len + i;
             __nv_bfloat16 *orow = a.out + qrow * a.out_rs + (int64_t)h * D + v_col0;
@@ -403,15 +468,15 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             const float inv_l = empty ? 0.f : 1.f / l_sum;
             if (n_tiles > 0) {
 #pragma unroll 1
-                for (int c = 0; c < C::kOCols; c += 16) {
+                for (int c = 16 * wg; c < C::kOCols; c += 32) {
                     uint32_t ov[16];
                     tmem_ld16(lane_base + kTmemO + c, ov);  // warp-wide: every lane takes part
                     tc_wait_ld();
                     uint32_t pk[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
-                                            __uint_as_float(ov[2 * e + 1]) * inv_l);
+                    for (int k = 0; k < 8; ++k)
+                        pk[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv_l,
+                                            __uint_as_float(ov[2 * k + 1]) * inv_l);
                     if (live) {
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
                         dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -419,9 +484,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     }
                 }
             } else if (live) {
-                for (int c = 0; c < C::kOCols; ++c) orow[c] = __float2bfloat16_rn(0.f);
+                for (int c = 16 * wg; c < C::kOCols; c += 32)
+                    for (int k = 0; k < 16; ++k) orow[c + k] = __float2bfloat16_rn(0.f);
             }
-            if (live && a.lse != nullptr && half == 0)
+            if (live && wg == 0 && a.lse != nullptr && half == 0)
                 a.lse[qrow * a.n_heads + h] =
                     empty ? -INFINITY : (m_ref + log2f(l_sum)) * 0.69314718055994531f;
         }
