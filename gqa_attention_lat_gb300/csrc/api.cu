@@ -55,6 +55,25 @@ bool make_head_map(CUtensorMap *m, const void *base, int head_dim, int heads, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map over a KV cache: (head-dim d, KV head, row < rows, sequence) with the
+// cache's own element strides, a [64, 1, box_rows, 1] box and 128-byte swizzle.
+bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int heads, int rows,
+                    int batch, int64_t row_stride, int64_t head_stride, int64_t seq_stride,
+                    int box_rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows,
+                                (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_stride * 2, (cuuint64_t)row_stride * 2,
+                                   (cuuint64_t)seq_stride * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int current_sm_count(int *out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -256,6 +275,14 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
         return LAT_ERR_WORKSPACE;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     lat::DecodeArgs a{};
+    if (max_kv_len > 0) {
+        const int box = lat::decode_bf16_tile_keys(head_dim);
+        if (!make_cache_map(&a.tm_k, k_cache, head_dim, n_kv_heads, max_kv_len, batch, cache_rs,
+                            cache_head_stride, cache_seq_stride, box) ||
+            !make_cache_map(&a.tm_v, v_cache, head_dim, n_kv_heads, max_kv_len, batch, cache_rs,
+                            cache_head_stride, cache_seq_stride, box))
+            return LAT_ERR_CUDA;
+    }
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.q_rs = q_rs;
     a.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);

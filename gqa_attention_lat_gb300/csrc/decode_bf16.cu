@@ -12,17 +12,23 @@
 //    chunk of one sequence's keys for one KV head, and serves ALL query heads of that
 //    GQA group from the same K/V bytes (up to 8 heads per head block), so each cached
 //    element is read from HBM once per decode step.
-//  * K/V rows arrive through a multi-stage cp.async ring of 16-byte copies (coalesced
-//    128-bit loads), XOR-swizzled in shared memory for conflict-free ldmatrix.
+//  * One producer thread streams K and V tiles with TMA (a 4-D tensor map over the
+//    cache's (head-dim, head, row, sequence) strides, 128-byte swizzled 64-column
+//    chunks) into a ring of stages guarded by mbarriers; the compute warps only run
+//    ldmatrix + mma.  Rows past the visible range are masked in S and, on the ragged
+//    last tile, zeroed in V by the warp that owns them (cache slots there may hold NaN).
 //  * The contraction runs on the tensor cores with keys in the M dimension:
 //      S^T[16 keys x 8 heads]   = K[16 x D] . Q^T[D x 8]        (mma m16n8k16)
 //      O^T[D x 8 heads]        += V^T[D x 16 keys] . P^T[16 x 8]
 //    so a GQA group of 8 heads fills the N=8 operand exactly.  P^T's fragment comes from
 //    S^T's accumulator by an in-register 8x8 transpose (movmatrix).
-//  * Each warp owns 16 keys of every tile and keeps its own running max/sum; the CTA's
+//  * Each warp owns 16 keys of every tile and keeps its own running max/sum, refreshed
+//    only when the max grows by more than 2^8 (so the O rescale is rare); the CTA's
 //    warps are merged through shared memory, and the splits of one (sequence, KV head)
 //    are merged by log-sum-exp by whichever CTA arrives last (an atomic ticket), so a
 //    decode step is one launch.
+//  * Every mbarrier wait is bounded; on expiry the CTA records LAT_ERR_TIMEOUT, drains
+//    its in-flight copies and skips its output.
 #include <math.h>
 
 #include <algorithm>
@@ -35,37 +41,53 @@ namespace lat {
 namespace {
 
 constexpr int kHeadsPerBlock = 8;  // N of the mma: query heads served per CTA
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint64_t kTimeoutNs = 4000000000ull;
 
 template <int D>
 struct DecodeCfg {
-    static constexpr int kWarps = D >= 256 ? 2 : 4;
-    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int kWarps = D >= 256 ? 2 : 4;           // compute warps
+    static constexpr int kThreads = 32 * (kWarps + 1);        // + one producer warp
     static constexpr int kTile = 16 * kWarps;                 // keys per pipeline stage
     static constexpr int kStages = D == 64 ? 4 : 3;
     static constexpr int kChunks = D / 8;                     // 16-byte chunks per row
-    static constexpr int kRowChunks = (kChunks + 7) / 8 * 8;  // padded for the swizzle
-    static constexpr int kRowBytes = kRowChunks * 16;
-    static constexpr int kQBytes = kHeadsPerBlock * kRowBytes;
-    static constexpr int kTileBytes = kTile * kRowBytes;
-    static constexpr int kSmem = kQBytes + kStages * 2 * kTileBytes;
-    // merge scratch (aliases the K/V ring after the main loop)
+    static constexpr int kCols64 = (D + 63) / 64;             // 64-column TMA chunks per row
+    static constexpr int kTileBytes = kCols64 * kTile * 128;  // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQRowChunks = (kChunks + 7) / 8 * 8; // Q rows padded for the swizzle
+    static constexpr int kQRowBytes = kQRowChunks * 16;
+    static constexpr int kQBytes = kHeadsPerBlock * kQRowBytes;
+    static constexpr int kBarBytes = 128;
+    static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStageBytes + kQBytes + kBarBytes;
+    // merge scratch (aliases the stage ring after the main loop)
     static constexpr int kMergeBytes = kWarps * (kHeadsPerBlock * D + 2 * kHeadsPerBlock) * 4;
-    static_assert(kMergeBytes <= kStages * 2 * kTileBytes, "merge scratch must fit the ring");
+    static_assert(kMergeBytes <= kStages * kStageBytes, "merge scratch must fit the ring");
+    static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-// byte offset of 16-byte chunk c of row r in a swizzled tile
-__device__ __forceinline__ uint32_t swz(int r, int c, int row_bytes) {
+// byte offset of 16-byte chunk c of row r in a tile stored as 64-column, 128-byte
+// swizzled regions of `rows` rows each (the TMA SWIZZLE_128B layout)
+__device__ __forceinline__ uint32_t tile_off(int r, int c, int rows) {
+    return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+// byte offset of 16-byte chunk c of Q row r (rows padded to a multiple of 8 chunks)
+__device__ __forceinline__ uint32_t q_off(int r, int c, int row_bytes) {
     return (uint32_t)(r * row_bytes + ((c ^ (r & 7)) << 4));
 }
 
 template <int D>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
-decode_bf16_kernel(const DecodeArgs a) {
+decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     using C = DecodeCfg<D>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *sQ = smem;
-    unsigned char *sKV = smem + C::kQBytes;  // [stage][K tile | V tile]
-    __shared__ int s_last;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sRing = smem;                                   // [stage][K tile | V tile]
+    unsigned char *sQ = smem + C::kStages * C::kStageBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sQ + C::kQBytes);  // [kStages]
+    uint64_t *empty = full + C::kStages;                           // [kStages]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + C::kStages);
+    int *s_last = const_cast<int *>(abort_flag + 1);
 
     const int split = blockIdx.x;
     const int HB = (a.n_heads / a.n_kv_heads + kHeadsPerBlock - 1) / kHeadsPerBlock;
@@ -98,130 +120,178 @@ decode_bf16_kernel(const DecodeArgs a) {
     const int kb = lo + split * a.chunk;
     const int ke = min(kv_len, kb + a.chunk);
     const int n_tiles = (ke - kb + C::kTile - 1) / C::kTile;
+    const uint64_t deadline = globaltimer_ns() + kTimeoutNs;
 
-    const __nv_bfloat16 *kbase = a.k_cache + (int64_t)b * a.cache_seq + (int64_t)hk * a.cache_head;
-    const __nv_bfloat16 *vbase = a.v_cache + (int64_t)b * a.cache_seq + (int64_t)hk * a.cache_head;
-
-    // ---- Q rows of this head block (rows >= g_cnt are zero) ------------------------
-    for (int i = tid; i < kHeadsPerBlock * C::kChunks; i += C::kThreads) {
-        const int g = i / C::kChunks, c = i % C::kChunks;
-        const bool ok = g < g_cnt;
-        const __nv_bfloat16 *src = a.q + (int64_t)b * a.q_rs + (int64_t)(h0 + (ok ? g : 0)) * D + c * 8;
-        cp_async_16(sQ + swz(g, c, C::kRowBytes), src, ok);
-    }
-
-    auto load_tile = [&](int t, int stage) {
-        unsigned char *dk = sKV + stage * 2 * C::kTileBytes;
-        unsigned char *dv = dk + C::kTileBytes;
-        const int key0 = kb + t * C::kTile;
-        for (int i = tid; i < C::kTile * C::kChunks; i += C::kThreads) {
-            const int r = i / C::kChunks, c = i % C::kChunks;
-            const int key = key0 + r;
-            const bool ok = key < ke;  // rows past the chunk are zero-filled, never read
-            const int64_t off = (int64_t)(ok ? key : kb) * a.cache_rs + c * 8;
-            cp_async_16(dk + swz(r, c, C::kRowBytes), kbase + off, ok);
-            cp_async_16(dv + swz(r, c, C::kRowBytes), vbase + off, ok);
+    if (tid == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::kWarps);
         }
-    };
-
-#pragma unroll
-    for (int s = 0; s < C::kStages - 1; ++s) {
-        if (s < n_tiles) load_tile(s, s);
-        cp_async_commit();
+        *abort_flag = 0;
+        fence_mbarrier_init();
     }
+    // Q rows of this head block (rows >= g_cnt are zero); the producer warp helps
+    for (int i = tid; i < kHeadsPerBlock * C::kQRowChunks; i += C::kThreads) {
+        const int g = i / C::kQRowChunks, c = i % C::kQRowChunks;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (g < g_cnt && c < C::kChunks)
+            v = *reinterpret_cast<const uint4 *>(a.q + (int64_t)b * a.q_rs + (int64_t)(h0 + g) * D + c * 8);
+        *reinterpret_cast<uint4 *>(sQ + q_off(g, c, C::kQRowBytes)) = v;
+    }
+    __syncthreads();
 
     // per-thread state: this thread's two head columns g0 = 2*(lane%4), g0+1
-    float m_run[2] = {-INFINITY, -INFINITY};
+    float m_ref[2] = {-INFINITY, -INFINITY};  // reference maxima (log2 domain, scaled)
     float l_run[2] = {0.f, 0.f};
     float acc[D / 16][4];
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-    for (int t = 0; t < n_tiles; ++t) {
-        cp_async_wait<C::kStages - 2>();
-        __syncthreads();
-        if (t + C::kStages - 1 < n_tiles) load_tile(t + C::kStages - 1, (t + C::kStages - 1) % C::kStages);
-        cp_async_commit();
-
-        const unsigned char *tk = sKV + (t % C::kStages) * 2 * C::kTileBytes;
-        const unsigned char *tv = tk + C::kTileBytes;
-        const int row0 = warp * 16;
-
-        // S^T = K . Q^T for this warp's 16 keys
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+    if (warp == C::kWarps) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&a.tm_k);
+            tma_prefetch_desc(&a.tm_v);
+            int last_issued[C::kStages];
+            for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int s = t % C::kStages;
+                if (!mbar_wait_bounded(&empty[s], ((t / C::kStages) & 1) ^ 1, abort_flag, deadline))
+                    break;
+                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                unsigned char *dk = sRing + s * C::kStageBytes;
+                unsigned char *dv = dk + C::kTileBytes;
+                const int key0 = kb + t * C::kTile;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ks += 2) {
-            uint32_t qf[4];  // b0,b1 for k-step ks and ks+1
-            {
-                const int r = lane & 7, c = 2 * ks + (lane >> 3);
-                ldmatrix_x4(qf, sQ + swz(r, c < C::kChunks ? c : 0, C::kRowBytes));
+                for (int c = 0; c < C::kCols64; ++c) {
+                    tma_load_4d(dk + c * C::kTile * 128, &a.tm_k, &full[s], c * 64, hk, key0, b);
+                    tma_load_4d(dv + c * C::kTile * 128, &a.tm_v, &full[s], c * 64, hk, key0, b);
+                }
+                last_issued[s] = t;
             }
+            // drain: every issued copy must land before the ring is reused or the CTA exits
+            const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
+            volatile int no_abort = 0;
+            for (int s = 0; s < C::kStages; ++s)
+                if (last_issued[s] >= 0)
+                    mbar_wait_bounded(&full[s], (last_issued[s] / C::kStages) & 1, &no_abort,
+                                      drain_deadline);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ compute warps
+        const int row0 = warp * 16;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % C::kStages;
+            const bool got = mbar_wait_bounded(&full[s], (t / C::kStages) & 1, abort_flag, deadline);
+            if (!__all_sync(0xffffffffu, got)) break;
+            unsigned char *tk = sRing + s * C::kStageBytes;
+            unsigned char *tv = tk + C::kTileBytes;
+            const int key0 = kb + t * C::kTile;
+            // this warp's rows past the chunk end: zero their V (their K is masked below)
+            const int valid_rows = ke - (key0 + row0);
+            if (valid_rows < 16) {
+                for (int i = lane; i < 16 * C::kChunks; i += 32) {
+                    const int r = i / C::kChunks, c = i % C::kChunks;
+                    if (r >= valid_rows)
+                        *reinterpret_cast<uint4 *>(tv + tile_off(row0 + r, c, C::kTile)) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+
+            // S^T = K . Q^T for this warp's 16 keys
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                if (ks + u < D / 16) {
-                    uint32_t af[4];
-                    const int r = row0 + (lane & 7) + 8 * ((lane >> 3) & 1);
-                    const int c = 2 * (ks + u) + (lane >> 4);
-                    ldmatrix_x4(af, tk + swz(r, c, C::kRowBytes));
-                    mma_bf16_16816(s, af, qf[2 * u], qf[2 * u + 1]);
+            for (int ks = 0; ks < D / 16; ks += 2) {
+                uint32_t qf[4];  // b0,b1 for k-step ks and ks+1
+                {
+                    const int r = lane & 7, c = 2 * ks + (lane >> 3);
+                    ldmatrix_x4(qf, sQ + q_off(r, c < C::kChunks ? c : 0, C::kQRowBytes));
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (ks + u < D / 16) {
+                        uint32_t af[4];
+                        const int r = row0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                        const int c = 2 * (ks + u) + (lane >> 4);
+                        ldmatrix_x4(af, tk + tile_off(r, c, C::kTile));
+                        mma_bf16_16816(sc, af, qf[2 * u], qf[2 * u + 1]);
+                    }
                 }
             }
-        }
-        // scale into the log2 domain and mask keys past the chunk
-        const int key_a = kb + t * C::kTile + row0 + (lane >> 2);
-        const bool va = key_a < ke, vb = key_a + 8 < ke;
-        s[0] = va ? s[0] * a.scale_log2 : -INFINITY;
-        s[1] = va ? s[1] * a.scale_log2 : -INFINITY;
-        s[2] = vb ? s[2] * a.scale_log2 : -INFINITY;
-        s[3] = vb ? s[3] * a.scale_log2 : -INFINITY;
+            // scale into the log2 domain and mask keys past the chunk
+            const int key_a = key0 + row0 + (lane >> 2);
+            const bool va = key_a < ke, vb = key_a + 8 < ke;
+            sc[0] = va ? sc[0] * a.scale_log2 : -INFINITY;
+            sc[1] = va ? sc[1] * a.scale_log2 : -INFINITY;
+            sc[2] = vb ? sc[2] * a.scale_log2 : -INFINITY;
+            sc[3] = vb ? sc[3] * a.scale_log2 : -INFINITY;
 
-        float p[4];
+            float p[4];
+            bool refresh_any = false;
+            float corr[2];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            float tmax = fmaxf(s[c], s[c + 2]);
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-            const float m_new = fmaxf(m_run[c], tmax);
-            const float m_ref = m_new == -INFINITY ? 0.f : m_new;  // no key seen yet
-            const float corr = fast_exp2(m_run[c] - m_ref);
-            p[c] = fast_exp2(s[c] - m_ref);
-            p[c + 2] = fast_exp2(s[c + 2] - m_ref);
-            l_run[c] = l_run[c] * corr + p[c] + p[c + 2];
-            m_run[c] = m_new;
+            for (int c = 0; c < 2; ++c) {
+                float tmax = fmaxf(sc[c], sc[c + 2]);
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+                // refresh the reference only when the max grew by more than the threshold
+                const bool refresh = tmax > m_ref[c] + kRescaleThreshold;
+                const float m_new = refresh ? tmax : m_ref[c];
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;  // no key seen yet
+                corr[c] = refresh ? fast_exp2(m_ref[c] - m_use) : 1.f;
+                p[c] = fast_exp2(sc[c] - m_use);
+                p[c + 2] = fast_exp2(sc[c + 2] - m_use);
+                l_run[c] = l_run[c] * corr[c] + p[c] + p[c + 2];
+                m_ref[c] = m_new;
+                refresh_any |= refresh;
+            }
+            if (__any_sync(0xffffffffu, refresh_any)) {
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) {
+                    acc[i][0] *= corr[0];
+                    acc[i][1] *= corr[1];
+                    acc[i][2] *= corr[0];
+                    acc[i][3] *= corr[1];
+                }
+            }
+            // P^T fragments: transpose the two 8x8 (key x head) quadrants
+            const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
+            const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
+            // O^T += V^T . P^T
 #pragma unroll
             for (int i = 0; i < D / 16; ++i) {
-                acc[i][c] *= corr;
-                acc[i][c + 2] *= corr;
+                uint32_t vf[4];
+                const int r = row0 + (lane & 7) + 8 * (lane >> 4);
+                const int c = 2 * i + ((lane >> 3) & 1);
+                ldmatrix_x4_trans(vf, tv + tile_off(r, c, C::kTile));
+                mma_bf16_16816(acc[i], vf, pb0, pb1);
             }
-        }
-        // P^T fragments: transpose the two 8x8 (key x head) quadrants
-        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
-        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
-        // O^T += V^T . P^T
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-            uint32_t vf[4];
-            const int r = row0 + (lane & 7) + 8 * (lane >> 4);
-            const int c = 2 * i + ((lane >> 3) & 1);
-            ldmatrix_x4_trans(vf, tv + swz(r, c, C::kRowBytes));
-            mma_bf16_16816(acc[i], vf, pb0, pb1);
+            // release the stage; zeroed rows (generic writes) must precede the next TMA
+            if (valid_rows < 16) fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
     }
-    cp_async_wait<0>();
     __syncthreads();  // the ring is free from here on: reuse it as merge scratch
+    if (*abort_flag) {
+        if (tid == 0) report_status(a.status, kErrTimeout);
+        return;
+    }
 
     // ---- merge the warps of this CTA ---------------------------------------------
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 4);
-        l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 8);
-        l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 16);
-    }
-    float *w_o = reinterpret_cast<float *>(sKV);                  // [warp][g][D]
+    float *w_o = reinterpret_cast<float *>(sRing);                // [warp][g][D]
     float *w_m = w_o + C::kWarps * kHeadsPerBlock * D;            // [warp][g]
     float *w_l = w_m + C::kWarps * kHeadsPerBlock;                // [warp][g]
-    {
+    if (warp < C::kWarps) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 4);
+            l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 8);
+            l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 16);
+        }
         const int g0 = 2 * (lane & 3);
         float *wo = w_o + warp * kHeadsPerBlock * D;
 #pragma unroll
@@ -233,8 +303,8 @@ decode_bf16_kernel(const DecodeArgs a) {
             wo[(g0 + 1) * D + d + 8] = acc[i][3];
         }
         if (lane < 4) {
-            w_m[warp * kHeadsPerBlock + g0] = m_run[0];
-            w_m[warp * kHeadsPerBlock + g0 + 1] = m_run[1];
+            w_m[warp * kHeadsPerBlock + g0] = m_ref[0];
+            w_m[warp * kHeadsPerBlock + g0 + 1] = m_ref[1];
             w_l[warp * kHeadsPerBlock + g0] = l_run[0];
             w_l[warp * kHeadsPerBlock + g0 + 1] = l_run[1];
         }
@@ -247,16 +317,17 @@ decode_bf16_kernel(const DecodeArgs a) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, w_m[w * kHeadsPerBlock + g]);
+        const float Mu = M == -INFINITY ? 0.f : M;
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < C::kWarps; ++w) {
-            const float f = fast_exp2(w_m[w * kHeadsPerBlock + g] - M);
+            const float f = fast_exp2(w_m[w * kHeadsPerBlock + g] - Mu);
             L += w_l[w * kHeadsPerBlock + g] * f;
             O += w_o[(w * kHeadsPerBlock + g) * D + d] * f;
         }
         const int h = h0 + g;
         const float o = O / L;
-        const float lse2 = M + log2f(L);  // log2-domain log-sum-exp of this chunk
+        const float lse2 = Mu + log2f(L);  // log2-domain log-sum-exp of this chunk
         if (single) {
             a.out[(int64_t)b * a.out_rs + (int64_t)h * D + d] = __float2bfloat16_rn(o);
             if (d == 0 && a.lse != nullptr) a.lse[(int64_t)b * a.n_heads + h] = lse2 * 0.69314718055994531f;
@@ -272,22 +343,22 @@ decode_bf16_kernel(const DecodeArgs a) {
     __threadfence();
     __syncthreads();
     int32_t *counter = a.counters + ((int64_t)b * a.n_kv_heads + hk) * HB + hb;
-    if (tid == 0) s_last = (atomicAdd(counter, 1) == n_splits - 1);
+    if (tid == 0) *s_last = (atomicAdd(counter, 1) == n_splits - 1);
     __syncthreads();
-    if (!s_last) return;
+    if (!*s_last) return;
     __threadfence();
 
-    float *wt = reinterpret_cast<float *>(sKV);           // [g][n_splits] weights
+    float *wt = reinterpret_cast<float *>(sRing);         // [g][n_splits] weights
     float *tot = wt + kHeadsPerBlock * n_splits;          // [g] merged log2-lse
-    for (int g = warp; g < g_cnt; g += C::kWarps) {
-        const int64_t row0 = ((int64_t)b * a.n_heads + h0 + g) * a.max_splits;
+    for (int g = warp; g < g_cnt; g += C::kWarps + 1) {
+        const int64_t rb = ((int64_t)b * a.n_heads + h0 + g) * a.max_splits;
         float M = -INFINITY;
-        for (int sp = lane; sp < n_splits; sp += 32) M = fmaxf(M, __ldcg(a.part_lse + row0 + sp));
+        for (int sp = lane; sp < n_splits; sp += 32) M = fmaxf(M, __ldcg(a.part_lse + rb + sp));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         float Z = 0.f;
         for (int sp = lane; sp < n_splits; sp += 32) {
-            const float e = fast_exp2(__ldcg(a.part_lse + row0 + sp) - M);
+            const float e = fast_exp2(__ldcg(a.part_lse + rb + sp) - M);
             wt[g * n_splits + sp] = e;
             Z += e;
         }
@@ -300,10 +371,10 @@ decode_bf16_kernel(const DecodeArgs a) {
     __syncthreads();
     for (int i = tid; i < g_cnt * D; i += C::kThreads) {
         const int g = i / D, d = i % D;
-        const int64_t row0 = ((int64_t)b * a.n_heads + h0 + g) * a.max_splits;
+        const int64_t rb = ((int64_t)b * a.n_heads + h0 + g) * a.max_splits;
         float o = 0.f;
         for (int sp = 0; sp < n_splits; ++sp)
-            o += wt[g * n_splits + sp] * __ldcg(a.part_o + (row0 + sp) * D + d);
+            o += wt[g * n_splits + sp] * __ldcg(a.part_o + (rb + sp) * D + d);
         a.out[(int64_t)b * a.out_rs + (int64_t)(h0 + g) * D + d] = __float2bfloat16_rn(o);
         if (d == 0 && a.lse != nullptr)
             a.lse[(int64_t)b * a.n_heads + h0 + g] = tot[g] * 0.69314718055994531f;
@@ -332,6 +403,17 @@ int ctas_per_sm() { return (228 * 1024) / (DecodeCfg<D>::kSmem + 1024); }
 
 }  // namespace
 
+int decode_bf16_tile_keys(int head_dim) {
+    switch (head_dim) {
+        case 64: return tile_keys<64>();
+        case 80: return tile_keys<80>();
+        case 128: return tile_keys<128>();
+        case 256: return tile_keys<256>();
+        case 512: return tile_keys<512>();
+        default: return 0;
+    }
+}
+
 bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
                       int window, int num_sms, DecodePlan *p) {
     int T, occ;
@@ -351,7 +433,7 @@ bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int 
     // The scratch layout depends on the window-free plan only, so a workspace sized by
     // lat_attn_decode_workspace_size fits every window.
     auto splits_for = [&](int rng) {
-        const int64_t target = (int64_t)num_sms * occ * 4;  // ~4 CTA waves for balance
+        const int64_t target = (int64_t)num_sms * occ * 2;  // ~2 CTA waves for balance
         int64_t sp = (target + units - 1) / std::max<int64_t>(units, 1);
         sp = std::min<int64_t>(sp, (rng + T - 1) / T);
         sp = std::min<int64_t>(sp, 512);

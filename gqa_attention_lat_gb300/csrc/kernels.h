@@ -43,6 +43,7 @@ cudaError_t launch_row_attention_f32(const RowAttnArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- bf16 split-KV decode
 struct DecodeArgs {
+    CUtensorMap tm_k, tm_v;  // 4-D maps (d, head, row < max_kv_len, sequence), 128-byte swizzle
     const __nv_bfloat16 *q;
     int64_t q_rs;
     const __nv_bfloat16 *k_cache, *v_cache;
@@ -68,6 +69,7 @@ struct DecodePlan {
 // Chooses the split size and the scratch layout; false when the shape is not built.
 bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
                       int window, int num_sms, DecodePlan *plan);
+int decode_bf16_tile_keys(int head_dim);     // cache rows per TMA box for this head_dim
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------- bf16 tensor-core prefill

@@ -120,8 +120,10 @@ size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int 
  *          range sets *status = LAT_ERR_BOUNDS and that row's output is left unwritten.
  *   out    element (b,h,d) at out[b*out_rs + h*head_dim + d], dtype dt
  *   lse    nullable fp32 [batch, n_heads]
- * max_kv_len is a host-side upper bound used to size the launch.  Cache slots at or
- * past kv_lens[b] are never read (they may hold anything, NaN included).
+ * max_kv_len is a host-side upper bound used to size the launch; every sequence's
+ * cache must hold at least max_kv_len rows (the kernel may load any row below
+ * max_kv_len in whole tiles).  Cache slots at or past kv_lens[b] never reach the result
+ * (they may hold anything, NaN included).
  * workspace: device scratch of at least lat_attn_decode_workspace_size(...) bytes,
  * 256-byte aligned; it must be zero-filled before its first use with a given layout
  * (the kernel returns its merge counters to zero, so later calls need no reset), and
