@@ -74,6 +74,21 @@ bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int heads, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over decode queries: (head-dim d, query head, sequence), 8-head boxes
+bool make_query_map(CUtensorMap *m, const void *base, int head_dim, int heads, int batch,
+                    int64_t row_stride) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)row_stride * 2};
+    const cuuint32_t box[3] = {64, 8, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int current_sm_count(int *out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -261,8 +276,8 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
         return lat::launch_row_attention_f32(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
     }
 
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || q_rs % 8 ||
-        cache_rs % 8 || cache_head_stride % 8 || cache_seq_stride % 8)
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        q_rs % 8 || cache_rs % 8 || cache_head_stride % 8 || cache_seq_stride % 8 || out_rs % 8)
         return LAT_ERR_INVALID_ARG;
     int sms = 0;
     if (!current_sm_count(&sms)) return LAT_ERR_CUDA;
@@ -280,7 +295,8 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
         if (!make_cache_map(&a.tm_k, k_cache, head_dim, n_kv_heads, max_kv_len, batch, cache_rs,
                             cache_head_stride, cache_seq_stride, box) ||
             !make_cache_map(&a.tm_v, v_cache, head_dim, n_kv_heads, max_kv_len, batch, cache_rs,
-                            cache_head_stride, cache_seq_stride, box))
+                            cache_head_stride, cache_seq_stride, box) ||
+            !make_query_map(&a.tm_q, q, head_dim, n_heads, batch, q_rs))
             return LAT_ERR_CUDA;
     }
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -305,9 +321,9 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
     a.part_lse = reinterpret_cast<float *>(ws + plan.part_o_bytes);
     a.counters = reinterpret_cast<int32_t *>(ws + plan.part_o_bytes + plan.part_lse_bytes);
     a.max_splits = plan.max_splits;
-    a.chunk = plan.chunk;
+    a.min_seg = plan.min_seg;
     a.status = status;
-    return lat::launch_decode_bf16(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
+    return lat::launch_decode_bf16(a, plan.grid, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
 }
 
 lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,

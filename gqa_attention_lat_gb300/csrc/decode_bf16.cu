@@ -8,27 +8,30 @@
 // page's fused kernel keeps in registers ("Current Design").
 //
 // How (GB300 design, not the pages'):
-//  * grid = (KV split, KV head x head block, sequence).  One CTA streams one contiguous
-//    chunk of one sequence's keys for one KV head, and serves ALL query heads of that
-//    GQA group from the same K/V bytes (up to 8 heads per head block), so each cached
-//    element is read from HBM once per decode step.
-//  * One producer thread streams K and V tiles with TMA (a 4-D tensor map over the
-//    cache's (head-dim, head, row, sequence) strides, 128-byte swizzled 64-column
-//    chunks) into a ring of stages guarded by mbarriers; the compute warps only run
-//    ldmatrix + mma.  Rows past the visible range are masked in S and, on the ragged
-//    last tile, zeroed in V by the warp that owns them (cache slots there may hold NaN).
+//  * Work unit = one (sequence, KV head, head block of <= 8 query heads): all query
+//    heads of a GQA group are served from the same K/V bytes, so each cached element is
+//    read from HBM once per decode step.
+//  * Persistent, statically balanced ("stream-K") schedule: the visible keys of all
+//    units, laid end to end, form one key stream; CTA c takes the c-th equal share of it
+//    (never less than a minimum stretch), which may cut units at both ends.  A CTA
+//    streams its share without draining its pipeline between units; a unit cut across
+//    CTAs leaves one partial (normalised output and log-sum-exp) per piece, merged by
+//    the CTA that finishes the unit's last piece (an atomic ticket), after its stream.
+//  * One producer thread streams K and V tiles with TMA (4-D tensor maps over the cache's
+//    (head-dim, head, row, sequence) strides, 128-byte swizzled 64-column chunks) into a
+//    ring of stages, each tagged with a record of what it holds; each unit's query rows
+//    arrive by TMA into a double buffer.  Rows past a piece's end are masked in S and, on
+//    its ragged last tile, zeroed in V by the warp that owns them (cache slots there may
+//    hold NaN).
 //  * The contraction runs on the tensor cores with keys in the M dimension:
 //      S^T[16 keys x 8 heads]   = K[16 x D] . Q^T[D x 8]        (mma m16n8k16)
 //      O^T[D x 8 heads]        += V^T[D x 16 keys] . P^T[16 x 8]
-//    so a GQA group of 8 heads fills the N=8 operand exactly.  P^T's fragment comes from
+//    so a GQA group of 8 heads fills the N=8 operand exactly; P^T's fragment comes from
 //    S^T's accumulator by an in-register 8x8 transpose (movmatrix).
 //  * Each warp owns 16 keys of every tile and keeps its own running max/sum, refreshed
-//    only when the max grows by more than 2^8 (so the O rescale is rare); the CTA's
-//    warps are merged through shared memory, and the splits of one (sequence, KV head)
-//    are merged by log-sum-exp by whichever CTA arrives last (an atomic ticket), so a
-//    decode step is one launch.
-//  * Every mbarrier wait is bounded; on expiry the CTA records LAT_ERR_TIMEOUT, drains
-//    its in-flight copies and skips its output.
+//    only when the max grows by more than 2^8 (so the O rescale is rare); at the end of
+//    a piece the warps' states meet in shared memory and warp 0 writes the result.
+//  * Every wait is bounded; on expiry the CTA records LAT_ERR_TIMEOUT and quits.
 #include <math.h>
 
 #include <algorithm>
@@ -40,9 +43,11 @@ namespace lat {
 
 namespace {
 
-constexpr int kHeadsPerBlock = 8;  // N of the mma: query heads served per CTA
+constexpr int kHeadsPerBlock = 8;          // N of the mma: query heads served per unit
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr int kMaxMerges = 2;              // multi-piece units a CTA can finish last
+constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
 struct DecodeCfg {
@@ -50,19 +55,35 @@ struct DecodeCfg {
     static constexpr int kThreads = 32 * (kWarps + 1);        // + one producer warp
     static constexpr int kTile = 16 * kWarps;                 // keys per pipeline stage
     static constexpr int kStages = D == 64 ? 4 : 3;
+    static constexpr int kMinBlocks = D == 512 ? 1 : (D == 64 ? 3 : 2);  // CTAs per SM
     static constexpr int kChunks = D / 8;                     // 16-byte chunks per row
     static constexpr int kCols64 = (D + 63) / 64;             // 64-column TMA chunks per row
     static constexpr int kTileBytes = kCols64 * kTile * 128;  // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kQRowChunks = (kChunks + 7) / 8 * 8; // Q rows padded for the swizzle
-    static constexpr int kQRowBytes = kQRowChunks * 16;
-    static constexpr int kQBytes = kHeadsPerBlock * kQRowBytes;
-    static constexpr int kBarBytes = 128;
-    static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStageBytes + kQBytes + kBarBytes;
-    // merge scratch (aliases the stage ring after the main loop)
-    static constexpr int kMergeBytes = kWarps * (kHeadsPerBlock * D + 2 * kHeadsPerBlock) * 4;
-    static_assert(kMergeBytes <= kStages * kStageBytes, "merge scratch must fit the ring");
+    static constexpr int kQBytes = kCols64 * kHeadsPerBlock * 128;   // 8 query rows
+    static constexpr int kMiscBytes = 640;                           // records, barriers, flags
+    static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStageBytes + 2 * kQBytes +
+                                 kMiscBytes;
     static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(kHeadsPerBlock * 66 * 4 + 64 <= kStages * kStageBytes, "merge weights");
+    static_assert(256 + (2 * kStages + 6) * 8 + 24 + 8 + 8 * 4 + kWarps * 2 * 16 <= kMiscBytes,
+                  "misc area");
+    // a warp's parked piece state fits in its own 16 rows of a stage's K and V tiles
+    static constexpr int kParkML = kHeadsPerBlock * D;        // accumulators, then m[8], l[8]
+    static constexpr int kHpw = kHeadsPerBlock / kWarps;      // heads each warp merges
+    static_assert(kParkML + 2 * kHeadsPerBlock <= 2 * kCols64 * 512, "parked state");
+    static_assert(kHeadsPerBlock % kWarps == 0, "merge split");
+};
+
+struct StageRec {
+    int b, hk, hb;      // unit
+    int key0;           // cache row of the tile's first key
+    int ke;             // end (exclusive) of the piece's keys
+    int first, last;    // first / last tile of the piece
+    int kq;             // piece number within this CTA (selects the query buffer)
+    int slot, nseg;     // partial slot of the piece, pieces of the unit
+    int end;            // no more tiles
+    int pad;
 };
 
 // byte offset of 16-byte chunk c of row r in a tile stored as 64-column, 128-byte
@@ -70,131 +91,278 @@ struct DecodeCfg {
 __device__ __forceinline__ uint32_t tile_off(int r, int c, int rows) {
     return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
-// byte offset of 16-byte chunk c of Q row r (rows padded to a multiple of 8 chunks)
-__device__ __forceinline__ uint32_t q_off(int r, int c, int row_bytes) {
-    return (uint32_t)(r * row_bytes + ((c ^ (r & 7)) << 4));
+
+struct SeqKeys {  // visible keys of one sequence
+    int lo, n;
+};
+__device__ __forceinline__ SeqKeys seq_keys_of(const DecodeArgs &a, int kv_len) {
+    SeqKeys s;
+    if (kv_len < 0 || kv_len > a.max_kv_len) {  // reported once, by CTA 0
+        s.lo = 0;
+        s.n = 0;
+        return s;
+    }
+    s.lo = a.window > 0 ? max(0, kv_len - a.window) : 0;
+    s.n = kv_len - s.lo;
+    return s;
+}
+__device__ __forceinline__ SeqKeys seq_keys(const DecodeArgs &a, int b) {
+    return seq_keys_of(a, a.kv_lens[b]);
 }
 
 template <int D>
-__global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
+__global__ void __launch_bounds__(DecodeCfg<D>::kThreads, DecodeCfg<D>::kMinBlocks)
 decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     using C = DecodeCfg<D>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *sRing = smem;                                   // [stage][K tile | V tile]
-    unsigned char *sQ = smem + C::kStages * C::kStageBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sQ + C::kQBytes);  // [kStages]
-    uint64_t *empty = full + C::kStages;                           // [kStages]
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + C::kStages);
-    int *s_last = const_cast<int *>(abort_flag + 1);
+    unsigned char *sRing = smem;                                          // [stage][K | V]
+    unsigned char *sQ = sRing + C::kStages * C::kStageBytes;              // [2] query blocks
+    unsigned char *misc = sQ + 2 * C::kQBytes;
+    StageRec *rec = reinterpret_cast<StageRec *>(misc);                   // [kStages]
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc + 256);            // [kStages]
+    uint64_t *empty = full + C::kStages;                                  // [kStages]
+    uint64_t *q_full = empty + C::kStages;                                // [2]
+    uint64_t *q_empty = q_full + 2;                                       // [2]
+    uint64_t *parked = q_empty + 2;                                       // piece states parked
+    long long *total_p = reinterpret_cast<long long *>(parked + 2);       // key-stream length
+    long long *start_p = total_p + 1;                                     // first sequence's offset
+    int *start_b = reinterpret_cast<int *>(start_p + 1);                  // CTA's first sequence
+    volatile int *abort_flag = start_b + 1;
+    int *n_merge = const_cast<int *>(abort_flag + 1);
+    int *merge_unit = n_merge + 1;                                        // [kMaxMerges][4]
+    int *tickets = merge_unit + 4 * kMaxMerges;                           // [kWarps][2][4]
+    // per-thread key counts; the ring is free until the first copy is issued
+    long long *scan = reinterpret_cast<long long *>(sRing);               // [warps] totals
 
-    const int split = blockIdx.x;
-    const int HB = (a.n_heads / a.n_kv_heads + kHeadsPerBlock - 1) / kHeadsPerBlock;
-    const int hk = blockIdx.y / HB, hb = blockIdx.y % HB;
-    const int b = blockIdx.z;
-    const int G = a.n_heads / a.n_kv_heads;
-    const int g_base = hb * kHeadsPerBlock;
-    const int g_cnt = min(kHeadsPerBlock, G - g_base);
-    const int h0 = hk * G + g_base;  // first query head of this block
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int HB = (G + kHeadsPerBlock - 1) / kHeadsPerBlock;
+    const int HU = a.n_kv_heads * HB;  // units per sequence
 
-    const int kv_len = a.kv_lens[b];
-    if (kv_len < 0 || kv_len > a.max_kv_len) {
-        if (split == 0 && hk == 0 && hb == 0 && tid == 0) report_status(a.status, kErrBounds);
-        return;
+    // ---- the tile stream: unit u of a sequence with n visible keys contributes
+    // ceil(n / kTile) tiles, units laid end to end; per-thread sums over a slice of the
+    // sequences, then a block-wide exclusive scan --------------------------------------
+    constexpr int T = C::kTile;
+    const int per_thread = (a.batch + C::kThreads - 1) / C::kThreads;
+    const int b_lo = min(a.batch, tid * per_thread), b_hi = min(a.batch, b_lo + per_thread);
+    if (tid == 0) {
+        *start_b = -1;
+        *start_p = 0;
     }
-    const int lo = a.window > 0 ? max(0, kv_len - a.window) : 0;  // keys lo .. kv_len-1
-    const int n_keys = kv_len - lo;
-    const int n_splits = (n_keys + a.chunk - 1) / a.chunk;
-    if (n_keys == 0) {  // nothing visible: out = 0, lse = -inf
-        if (split == 0) {
-            for (int i = tid; i < g_cnt * D; i += blockDim.x)
-                a.out[(int64_t)b * a.out_rs + (int64_t)(h0 + i / D) * D + i % D] =
-                    __float2bfloat16_rn(0.f);
-            if (a.lse != nullptr && tid < g_cnt) a.lse[(int64_t)b * a.n_heads + h0 + tid] = -INFINITY;
+    long long my_sum = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int kv_len = a.kv_lens[b];
+        const SeqKeys sk = seq_keys_of(a, kv_len);
+        my_sum += (long long)((sk.n + T - 1) / T) * HU;
+        if (blockIdx.x == 0) {  // CTA 0 handles sequences with nothing to stream
+            if (kv_len < 0 || kv_len > a.max_kv_len) {
+                report_status(a.status, kErrBounds);
+            } else if (sk.n == 0) {
+                for (int i = 0; i < a.n_heads * D; ++i)
+                    a.out[(int64_t)b * a.out_rs + i] = __float2bfloat16_rn(0.f);
+                if (a.lse != nullptr)
+                    for (int h = 0; h < a.n_heads; ++h) a.lse[(int64_t)b * a.n_heads + h] = -INFINITY;
+            }
         }
-        return;
     }
-    if (split >= n_splits) return;
-    const int kb = lo + split * a.chunk;
-    const int ke = min(kv_len, kb + a.chunk);
-    const int n_tiles = (ke - kb + C::kTile - 1) / C::kTile;
-    const uint64_t deadline = globaltimer_ns() + kTimeoutNs;
-
+    long long incl = my_sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    long long total = 0, my_start = incl - my_sum;
+#pragma unroll
+    for (int w = 0; w < C::kWarps + 1; ++w) {
+        const long long v = scan[w];
+        if (w < warp) my_start += v;
+        total += v;
+    }
+    const long long per_cta = max((total + gridDim.x - 1) / gridDim.x, (long long)(a.min_seg / T));
+    const long long r0 = (long long)blockIdx.x * per_cta;
+    const long long r1 = min(total, r0 + per_cta);
+    const bool has_work = r0 < total;
+    if (has_work && r0 >= my_start && r0 < my_start + my_sum) {  // r0 is in this slice
+        long long p = my_start;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const SeqKeys sk = seq_keys(a, b);
+            const long long w = (long long)((sk.n + T - 1) / T) * HU;
+            if (r0 >= p && r0 < p + w) {
+                *start_b = b;
+                *start_p = p;
+            }
+            p += w;
+        }
+    }
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], C::kWarps);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], C::kWarps);
+        }
+        mbar_init(parked, C::kWarps);
         *abort_flag = 0;
+        *n_merge = 0;
         fence_mbarrier_init();
     }
-    // Q rows of this head block (rows >= g_cnt are zero); the producer warp helps
-    for (int i = tid; i < kHeadsPerBlock * C::kQRowChunks; i += C::kThreads) {
-        const int g = i / C::kQRowChunks, c = i % C::kQRowChunks;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (g < g_cnt && c < C::kChunks)
-            v = *reinterpret_cast<const uint4 *>(a.q + (int64_t)b * a.q_rs + (int64_t)(h0 + g) * D + c * 8);
-        *reinterpret_cast<uint4 *>(sQ + q_off(g, c, C::kQRowBytes)) = v;
-    }
+    fence_proxy_async_smem();  // the scan's generic writes precede the ring's first copies
     __syncthreads();
-
-    // per-thread state: this thread's two head columns g0 = 2*(lane%4), g0+1
-    float m_ref[2] = {-INFINITY, -INFINITY};  // reference maxima (log2 domain, scaled)
-    float l_run[2] = {0.f, 0.f};
-    float acc[D / 16][4];
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    const uint64_t deadline = globaltimer_ns() + kTimeoutNs;
 
     if (warp == C::kWarps) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&a.tm_k);
             tma_prefetch_desc(&a.tm_v);
-            int last_issued[C::kStages];
-            for (int s = 0; s < C::kStages; ++s) last_issued[s] = -1;
-            for (int t = 0; t < n_tiles; ++t) {
-                const int s = t % C::kStages;
-                if (!mbar_wait_bounded(&empty[s], ((t / C::kStages) & 1) ^ 1, abort_flag, deadline))
-                    break;
-                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                unsigned char *dk = sRing + s * C::kStageBytes;
-                unsigned char *dv = dk + C::kTileBytes;
-                const int key0 = kb + t * C::kTile;
-#pragma unroll
-                for (int c = 0; c < C::kCols64; ++c) {
-                    tma_load_4d(dk + c * C::kTile * 128, &a.tm_k, &full[s], c * 64, hk, key0, b);
-                    tma_load_4d(dv + c * C::kTile * 128, &a.tm_v, &full[s], c * 64, hk, key0, b);
+            tma_prefetch_desc(&a.tm_q);
+            int tg = 0, kq = 0;  // stage fills issued, query blocks issued
+            bool ok = true;
+            if (has_work && *start_b >= 0) {
+                int b = *start_b;
+                long long pb = *start_p;  // stream offset of sequence b's first unit
+                long long pos = r0;
+                SeqKeys sk = seq_keys(a, b);
+                int next_len = b + 1 < a.batch ? a.kv_lens[b + 1] : 0;  // fetched ahead
+                while (pos < r1 && ok) {
+                    const int nt = (sk.n + T - 1) / T;
+                    const long long w = (long long)nt * HU;
+                    if (pos >= pb + w) {  // nothing (left) of this sequence in our share
+                        pb += w;
+                        if (++b >= a.batch) break;
+                        sk = seq_keys_of(a, next_len);
+                        next_len = b + 1 < a.batch ? a.kv_lens[b + 1] : 0;
+                        continue;
+                    }
+                    const int idx = (int)((pos - pb) / nt);  // unit within the sequence
+                    const int hk = idx / HB, hb = idx % HB;
+                    const long long ustart = pb + (long long)idx * nt;
+                    const int t0 = (int)(pos - ustart);
+                    const int t1 = (int)min((long long)nt, r1 - ustart);
+                    const long long first_cta = ustart / per_cta;
+                    const long long last_cta = (ustart + nt - 1) / per_cta;
+                    const int nseg = (int)(last_cta - first_cta + 1);
+                    const int slot = (int)(blockIdx.x - first_cta);
+                    // query rows of the unit's heads
+                    const int qs = kq & 1;
+                    if (!mbar_wait_bounded(&q_empty[qs], ((kq >> 1) & 1) ^ 1, abort_flag, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
+                    const int h0 = hk * G + hb * kHeadsPerBlock;
+                    for (int c = 0; c < C::kCols64; ++c)
+                        tma_load_3d(sQ + qs * C::kQBytes + c * kHeadsPerBlock * 128, &a.tm_q,
+                                    &q_full[qs], c * 64, h0, b);
+                    const int kbeg = sk.lo + t0 * T;
+                    const int kend = sk.lo + min(sk.n, t1 * T);
+                    for (int key0 = kbeg; key0 < kend; key0 += T) {
+                        const int s = tg % C::kStages;
+                        if (!mbar_wait_bounded(&empty[s], ((tg / C::kStages) & 1) ^ 1, abort_flag,
+                                               deadline)) {
+                            ok = false;
+                            break;
+                        }
+                        StageRec r;
+                        r.b = b; r.hk = hk; r.hb = hb; r.key0 = key0; r.ke = kend;
+                        r.first = key0 == kbeg; r.last = key0 + T >= kend;
+                        r.kq = kq; r.slot = slot; r.nseg = nseg; r.end = 0; r.pad = 0;
+                        rec[s] = r;
+                        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                        unsigned char *dk = sRing + s * C::kStageBytes;
+                        unsigned char *dv = dk + C::kTileBytes;
+                        for (int c = 0; c < C::kCols64; ++c) {
+                            tma_load_4d(dk + c * C::kTile * 128, &a.tm_k, &full[s], c * 64, hk, key0, b);
+                            tma_load_4d(dv + c * C::kTile * 128, &a.tm_v, &full[s], c * 64, hk, key0, b);
+                        }
+                        ++tg;
+                    }
+                    ++kq;
+                    pos = ustart + t1;
                 }
-                last_issued[s] = t;
             }
-            // drain: every issued copy must land before the ring is reused or the CTA exits
+            if (ok) {  // end-of-stream record
+                const int s = tg % C::kStages;
+                if (mbar_wait_bounded(&empty[s], ((tg / C::kStages) & 1) ^ 1, abort_flag, deadline)) {
+                    rec[s].end = 1;
+                    mbar_arrive(&full[s]);
+                    ++tg;  // the drain must wait on this phase, not an older one
+                }
+            }
+            // drain: every issued copy must land before the CTA may exit.  Fills go round
+            // the ring in order, so stage s last held fill s + k*kStages, the largest below tg.
             const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
             volatile int no_abort = 0;
+#pragma unroll
             for (int s = 0; s < C::kStages; ++s)
-                if (last_issued[s] >= 0)
-                    mbar_wait_bounded(&full[s], (last_issued[s] / C::kStages) & 1, &no_abort,
-                                      drain_deadline);
+                if (s < tg) {
+                    const int last = s + (tg - 1 - s) / C::kStages * C::kStages;
+                    mbar_wait_bounded(&full[s], (last / C::kStages) & 1, &no_abort, drain_deadline);
+                }
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (i < kq) {
+                    const int last = i + (kq - 1 - i) / 2 * 2;
+                    mbar_wait_bounded(&q_full[i], (last >> 1) & 1, &no_abort, drain_deadline);
+                }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ compute warps
         const int row0 = warp * 16;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % C::kStages;
-            const bool got = mbar_wait_bounded(&full[s], (t / C::kStages) & 1, abort_flag, deadline);
+        float m_ref[2] = {-INFINITY, -INFINITY};  // reference maxima (log2 domain, scaled)
+        float l_run[2] = {0.f, 0.f};
+        float acc[D / 16][4];
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        int mk = 0;  // pieces finished
+        constexpr int kParkML = C::kParkML, kHpw = C::kHpw;
+        // float f of warp w's parked state: 512 floats per 64-column chunk of its 16 rows,
+        // K tile chunks first, then V tile chunks
+        auto park_at = [](unsigned char *tk_, unsigned char *tv_, int w, int f) -> float * {
+            const int p = f >> 9;
+            unsigned char *base = p < C::kCols64 ? tk_ + p * C::kTile * 128
+                                                 : tv_ + (p - C::kCols64) * C::kTile * 128;
+            return reinterpret_cast<float *>(base + w * 16 * 128) + (f & 511);
+        };
+        // split pieces' merge tickets (at most two per CTA: its first and last piece), kept
+        // as {ticket, nseg | unit << 8, b, h_base | g_cnt << 24}
+        int n_tickets = 0;
+        int *my_tickets = tickets + warp * 8;
+        for (int tg = 0;; ++tg) {
+            const int s = tg % C::kStages;
+            const bool got = mbar_wait_bounded(&full[s], (tg / C::kStages) & 1, abort_flag, deadline);
             if (!__all_sync(0xffffffffu, got)) break;
+            const StageRec r = rec[s];
+            if (r.end) break;
+            const int qs = r.kq & 1;
+            if (r.first) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    m_ref[c] = -INFINITY;
+                    l_run[c] = 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+                const bool qgot = mbar_wait_bounded(&q_full[qs], (r.kq >> 1) & 1, abort_flag, deadline);
+                if (!__all_sync(0xffffffffu, qgot)) break;
+            }
             unsigned char *tk = sRing + s * C::kStageBytes;
             unsigned char *tv = tk + C::kTileBytes;
-            const int key0 = kb + t * C::kTile;
-            // this warp's rows past the chunk end: zero their V (their K is masked below)
-            const int valid_rows = ke - (key0 + row0);
+            const unsigned char *tq = sQ + qs * C::kQBytes;
+            // this warp's rows past the piece's end: zero their V (their K is masked below)
+            const int valid_rows = r.ke - (r.key0 + row0);
             if (valid_rows < 16) {
                 for (int i = lane; i < 16 * C::kChunks; i += 32) {
-                    const int r = i / C::kChunks, c = i % C::kChunks;
-                    if (r >= valid_rows)
-                        *reinterpret_cast<uint4 *>(tv + tile_off(row0 + r, c, C::kTile)) =
+                    const int rr = i / C::kChunks, c = i % C::kChunks;
+                    if (rr >= valid_rows)
+                        *reinterpret_cast<uint4 *>(tv + tile_off(row0 + rr, c, C::kTile)) =
                             make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
@@ -204,33 +372,32 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < D / 16; ks += 2) {
-                uint32_t qf[4];  // b0,b1 for k-step ks and ks+1
+                uint32_t qf[4];  // b0,b1 for k-steps ks and ks+1
                 {
-                    const int r = lane & 7, c = 2 * ks + (lane >> 3);
-                    ldmatrix_x4(qf, sQ + q_off(r, c < C::kChunks ? c : 0, C::kQRowBytes));
+                    const int c = 2 * ks + (lane >> 3);
+                    ldmatrix_x4(qf, tq + tile_off(lane & 7, c < C::kChunks ? c : 0, kHeadsPerBlock));
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     if (ks + u < D / 16) {
                         uint32_t af[4];
-                        const int r = row0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                        const int rr = row0 + (lane & 7) + 8 * ((lane >> 3) & 1);
                         const int c = 2 * (ks + u) + (lane >> 4);
-                        ldmatrix_x4(af, tk + tile_off(r, c, C::kTile));
+                        ldmatrix_x4(af, tk + tile_off(rr, c, C::kTile));
                         mma_bf16_16816(sc, af, qf[2 * u], qf[2 * u + 1]);
                     }
                 }
             }
-            // scale into the log2 domain and mask keys past the chunk
-            const int key_a = key0 + row0 + (lane >> 2);
-            const bool va = key_a < ke, vb = key_a + 8 < ke;
+            // scale into the log2 domain and mask keys past the piece
+            const int key_a = r.key0 + row0 + (lane >> 2);
+            const bool va = key_a < r.ke, vb = key_a + 8 < r.ke;
             sc[0] = va ? sc[0] * a.scale_log2 : -INFINITY;
             sc[1] = va ? sc[1] * a.scale_log2 : -INFINITY;
             sc[2] = vb ? sc[2] * a.scale_log2 : -INFINITY;
             sc[3] = vb ? sc[3] * a.scale_log2 : -INFINITY;
 
-            float p[4];
+            float p[4], corr[2];
             bool refresh_any = false;
-            float corr[2];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float tmax = fmaxf(sc[c], sc[c + 2]);
@@ -264,134 +431,202 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
 #pragma unroll
             for (int i = 0; i < D / 16; ++i) {
                 uint32_t vf[4];
-                const int r = row0 + (lane & 7) + 8 * (lane >> 4);
+                const int rr = row0 + (lane & 7) + 8 * (lane >> 4);
                 const int c = 2 * i + ((lane >> 3) & 1);
-                ldmatrix_x4_trans(vf, tv + tile_off(r, c, C::kTile));
+                ldmatrix_x4_trans(vf, tv + tile_off(rr, c, C::kTile));
                 mma_bf16_16816(acc[i], vf, pb0, pb1);
             }
-            // release the stage; zeroed rows (generic writes) must precede the next TMA
+            // zeroed rows (generic writes) must precede the stage's next copy
             if (valid_rows < 16) fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (!r.last) {  // release the stage
+                if (lane == 0) mbar_arrive(&empty[s]);
+                continue;
+            }
+
+            // ---- end of a piece: release the query block, merge the warps ----------
+            // Every warp parks its state in its own rows of this stage, which no other warp
+            // reads while computing: accumulator register j = 4i+e of lane l at float
+            // 32j + (l ^ (j & 31)) (the XOR spreads the merge's reads over the banks), then
+            // m[8] and l[8].  Once all warps have parked, warp w combines heads
+            // [w*kHpw, (w+1)*kHpw) of every state, writes them out and releases the stage.
+            if (lane == 0) mbar_arrive(&q_empty[qs]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 4);
+                l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 8);
+                l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 16);
+            }
+            {
+                const int g0 = 2 * (lane & 3);
+#pragma unroll
+                for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 4 * i + e;
+                        *park_at(tk, tv, warp, 32 * j + (lane ^ (j & 31))) = acc[i][e];
+                    }
+                if (lane < 4) {
+                    float *ml = park_at(tk, tv, warp, kParkML);
+                    ml[g0] = m_ref[0];
+                    ml[g0 + 1] = m_ref[1];
+                    ml[kHeadsPerBlock + g0] = l_run[0];
+                    ml[kHeadsPerBlock + g0 + 1] = l_run[1];
+                }
+            }
+            fence_proxy_async_smem();  // the parked writes precede the stage's next copy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(parked);
+            const bool pk = mbar_wait_bounded(parked, mk & 1, abort_flag, deadline);
+            if (!__all_sync(0xffffffffu, pk)) break;
+
+            const int h_base = r.hk * G + r.hb * kHeadsPerBlock;
+            const int g_cnt = min(kHeadsPerBlock, G - r.hb * kHeadsPerBlock);
+            const bool single = r.nseg == 1;
+            const int64_t prow = ((int64_t)r.b * a.n_heads + h_base) * a.max_splits + r.slot;
+            constexpr int kV8 = D / 8;  // 8-element vectors per head row
+            for (int v = lane; v < kHpw * kV8; v += 32) {
+                const int g = warp * kHpw + v / kV8, x = 8 * (v % kV8);
+                if (g >= g_cnt) continue;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < C::kWarps; ++w) mx = fmaxf(mx, park_at(tk, tv, w, kParkML)[g]);
+                const float mu = mx == -INFINITY ? 0.f : mx;
+                float f[C::kWarps], l = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::kWarps; ++w) {
+                    const float *ml = park_at(tk, tv, w, kParkML);
+                    f[w] = fast_exp2(ml[g] - mu);
+                    l += ml[kHeadsPerBlock + g] * f[w];
+                }
+                const float rl = 1.f / l;
+                // element (g, x+k) sits in register j = 4*(x/16) + (g&1) + 2*((x/8)&1) of
+                // lane 4k + g/2 (the m16n8 accumulator layout with keys' D in M)
+                const int j = 4 * (x >> 4) + (g & 1) + 2 * ((x >> 3) & 1);
+                float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int w = 0; w < C::kWarps; ++w) {
+                    const float *row = park_at(tk, tv, w, 32 * j);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) o[k] += f[w] * row[(4 * k + (g >> 1)) ^ (j & 31)];
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] *= rl;
+                const float lse2 = mu + log2f(l);  // log2 domain
+                if (single) {
+                    *reinterpret_cast<uint4 *>(a.out + (int64_t)r.b * a.out_rs +
+                                               (int64_t)(h_base + g) * D + x) =
+                        make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                   pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+                    if (x == 0 && a.lse != nullptr) a.lse[(int64_t)r.b * a.n_heads + h_base + g] = lse2 * kLn2;
+                } else {
+                    float *dst = a.part_o + (prow + (int64_t)g * a.max_splits) * D + x;
+                    *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<float4 *>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+                    if (x == 0) a.part_lse[prow + (int64_t)g * a.max_splits] = lse2;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+            if (!single) {
+                // Ticket: the warp that brings the unit's count to nseg * kWarps is the last
+                // writer of its partials and queues the unit for merging after the stream.
+                // The result is only examined after the stream, so the round trip overlaps it.
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    const int unit = (r.b * a.n_kv_heads + r.hk) * HB + r.hb;
+                    const int t = atomicAdd(a.counters + unit, 1);
+                    if (n_tickets < 2) {
+                        int *tk4 = my_tickets + 4 * n_tickets;
+                        tk4[0] = t;
+                        tk4[1] = r.nseg | (unit << 8);
+                        tk4[2] = r.b;
+                        tk4[3] = h_base | (g_cnt << 24);
+                    }
+                    ++n_tickets;
+                }
+            }
+            ++mk;
+        }
+        if (lane == 0) {  // queue the units whose last partial this warp wrote
+            if (n_tickets > 2) report_status(a.status, kErrCuda);  // cannot happen by construction
+            for (int k = 0; k < min(n_tickets, 2); ++k) {
+                const int *tk4 = my_tickets + 4 * k;
+                if (tk4[0] != (tk4[1] & 0xff) * C::kWarps - 1) continue;
+                const int n = atomicAdd(n_merge, 1);
+                if (n < kMaxMerges) {
+                    merge_unit[4 * n + 0] = tk4[2];
+                    merge_unit[4 * n + 1] = tk4[3] & 0xffffff;
+                    merge_unit[4 * n + 2] = tk4[3] >> 24;
+                    merge_unit[4 * n + 3] = tk4[1];
+                } else {
+                    report_status(a.status, kErrCuda);  // cannot happen by construction
+                }
+            }
         }
     }
-    __syncthreads();  // the ring is free from here on: reuse it as merge scratch
+    __syncthreads();
     if (*abort_flag) {
         if (tid == 0) report_status(a.status, kErrTimeout);
         return;
     }
 
-    // ---- merge the warps of this CTA ---------------------------------------------
-    float *w_o = reinterpret_cast<float *>(sRing);                // [warp][g][D]
-    float *w_m = w_o + C::kWarps * kHeadsPerBlock * D;            // [warp][g]
-    float *w_l = w_m + C::kWarps * kHeadsPerBlock;                // [warp][g]
-    if (warp < C::kWarps) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 4);
-            l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 8);
-            l_run[c] += __shfl_xor_sync(0xffffffffu, l_run[c], 16);
-        }
-        const int g0 = 2 * (lane & 3);
-        float *wo = w_o + warp * kHeadsPerBlock * D;
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-            const int d = 16 * i + (lane >> 2);
-            wo[g0 * D + d] = acc[i][0];
-            wo[(g0 + 1) * D + d] = acc[i][1];
-            wo[g0 * D + d + 8] = acc[i][2];
-            wo[(g0 + 1) * D + d + 8] = acc[i][3];
-        }
-        if (lane < 4) {
-            w_m[warp * kHeadsPerBlock + g0] = m_ref[0];
-            w_m[warp * kHeadsPerBlock + g0 + 1] = m_ref[1];
-            w_l[warp * kHeadsPerBlock + g0] = l_run[0];
-            w_l[warp * kHeadsPerBlock + g0 + 1] = l_run[1];
-        }
-    }
-    __syncthreads();
-
-    const bool single = n_splits == 1;
-    for (int i = tid; i < g_cnt * D; i += C::kThreads) {
-        const int g = i / D, d = i % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, w_m[w * kHeadsPerBlock + g]);
-        const float Mu = M == -INFINITY ? 0.f : M;
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) {
-            const float f = fast_exp2(w_m[w * kHeadsPerBlock + g] - Mu);
-            L += w_l[w * kHeadsPerBlock + g] * f;
-            O += w_o[(w * kHeadsPerBlock + g) * D + d] * f;
-        }
-        const int h = h0 + g;
-        const float o = O / L;
-        const float lse2 = Mu + log2f(L);  // log2-domain log-sum-exp of this chunk
-        if (single) {
-            a.out[(int64_t)b * a.out_rs + (int64_t)h * D + d] = __float2bfloat16_rn(o);
-            if (d == 0 && a.lse != nullptr) a.lse[(int64_t)b * a.n_heads + h] = lse2 * 0.69314718055994531f;
-        } else {
-            const int64_t row = ((int64_t)b * a.n_heads + h) * a.max_splits + split;
-            a.part_o[row * D + d] = o;
-            if (d == 0) a.part_lse[row] = lse2;
-        }
-    }
-    if (single) return;
-
-    // ---- the last CTA of this (sequence, KV head, head block) merges the splits ------
+    // ---- merge the units this CTA finished last: lse-weighted sum of their pieces ----
+    // One thread per 4 output elements; every partial it needs is loaded before any is
+    // used, so a merge costs about one round trip to L2.
     __threadfence();
-    __syncthreads();
-    int32_t *counter = a.counters + ((int64_t)b * a.n_kv_heads + hk) * HB + hb;
-    if (tid == 0) *s_last = (atomicAdd(counter, 1) == n_splits - 1);
-    __syncthreads();
-    if (!*s_last) return;
-    __threadfence();
-
-    float *wt = reinterpret_cast<float *>(sRing);         // [g][n_splits] weights
-    float *tot = wt + kHeadsPerBlock * n_splits;          // [g] merged log2-lse
-    for (int g = warp; g < g_cnt; g += C::kWarps + 1) {
-        const int64_t rb = ((int64_t)b * a.n_heads + h0 + g) * a.max_splits;
-        float M = -INFINITY;
-        for (int sp = lane; sp < n_splits; sp += 32) M = fmaxf(M, __ldcg(a.part_lse + rb + sp));
+    const int n_merges = min(*n_merge, kMaxMerges);
+    for (int mi = 0; mi < n_merges; ++mi) {
+        const int b = merge_unit[4 * mi + 0], h_base = merge_unit[4 * mi + 1];
+        const int g_cnt = merge_unit[4 * mi + 2];
+        const int nseg = merge_unit[4 * mi + 3] & 0xff, unit = merge_unit[4 * mi + 3] >> 8;
+        constexpr int kV4 = D / 4;
+        for (int i = tid; i < g_cnt * kV4; i += C::kThreads) {
+            const int g = i / kV4, x = 4 * (i % kV4);
+            const int64_t rb = ((int64_t)b * a.n_heads + h_base + g) * a.max_splits;
+            float M = -INFINITY, Z = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp0 = 0; sp0 < nseg; sp0 += 4) {  // four partials per batch of loads
+                float lv[4];
+                float4 ov[4];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float Z = 0.f;
-        for (int sp = lane; sp < n_splits; sp += 32) {
-            const float e = fast_exp2(__ldcg(a.part_lse + rb + sp) - M);
-            wt[g * n_splits + sp] = e;
-            Z += e;
+                for (int k = 0; k < 4; ++k) {
+                    const bool in = sp0 + k < nseg;
+                    lv[k] = in ? __ldcg(a.part_lse + rb + sp0 + k) : -INFINITY;
+                    ov[k] = in ? __ldcg(reinterpret_cast<const float4 *>(a.part_o + (rb + sp0 + k) * D + x))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                float mb = M;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mb = fmaxf(mb, lv[k]);
+                const float c = M == -INFINITY ? 0.f : fast_exp2(M - mb);  // rescale earlier batches
+                Z *= c;
+                o.x *= c; o.y *= c; o.z *= c; o.w *= c;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float e = lv[k] == -INFINITY ? 0.f : fast_exp2(lv[k] - mb);
+                    Z += e;
+                    o.x += e * ov[k].x; o.y += e * ov[k].y; o.z += e * ov[k].z; o.w += e * ov[k].w;
+                }
+                M = mb;
+            }
+            const float rz = 1.f / Z;
+            *reinterpret_cast<uint2 *>(a.out + (int64_t)b * a.out_rs + (int64_t)(h_base + g) * D + x) =
+                make_uint2(pack_bf16x2(o.x * rz, o.y * rz), pack_bf16x2(o.z * rz, o.w * rz));
+            if (x == 0 && a.lse != nullptr)
+                a.lse[(int64_t)b * a.n_heads + h_base + g] = (M + log2f(Z)) * kLn2;
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, off);
-        const float inv = 1.f / Z;
-        for (int sp = lane; sp < n_splits; sp += 32) wt[g * n_splits + sp] *= inv;
-        if (lane == 0) tot[g] = M + log2f(Z);
+        if (tid == 0) a.counters[unit] = 0;  // ready for the next call
     }
-    __syncthreads();
-    for (int i = tid; i < g_cnt * D; i += C::kThreads) {
-        const int g = i / D, d = i % D;
-        const int64_t rb = ((int64_t)b * a.n_heads + h0 + g) * a.max_splits;
-        float o = 0.f;
-        for (int sp = 0; sp < n_splits; ++sp)
-            o += wt[g * n_splits + sp] * __ldcg(a.part_o + (rb + sp) * D + d);
-        a.out[(int64_t)b * a.out_rs + (int64_t)(h0 + g) * D + d] = __float2bfloat16_rn(o);
-        if (d == 0 && a.lse != nullptr)
-            a.lse[(int64_t)b * a.n_heads + h0 + g] = tot[g] * 0.69314718055994531f;
-    }
-    if (tid == 0) *counter = 0;  // ready for the next call
 }
 
 template <int D>
-cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t s) {
+cudaError_t launch_decode_d(const DecodeArgs &a, int grid, cudaStream_t s) {
     using C = DecodeCfg<D>;
     cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    const int HB = (a.n_heads / a.n_kv_heads + kHeadsPerBlock - 1) / kHeadsPerBlock;
-    const int range = a.window > 0 ? min(a.max_kv_len, a.window) : a.max_kv_len;
-    const int grid_splits = max(1, (range + a.chunk - 1) / a.chunk);
-    dim3 grid(grid_splits, a.n_kv_heads * HB, a.batch);
     decode_bf16_kernel<D><<<grid, C::kThreads, C::kSmem, s>>>(a);
     return cudaGetLastError();
 }
@@ -399,7 +634,16 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t s) {
 template <int D>
 int tile_keys() { return DecodeCfg<D>::kTile; }
 template <int D>
-int ctas_per_sm() { return (228 * 1024) / (DecodeCfg<D>::kSmem + 1024); }
+int ctas_per_sm() {  // resident CTAs per SM as the runtime sees them (smem and registers)
+    using C = DecodeCfg<D>;
+    int n = 0;
+    if (cudaFuncSetAttribute(decode_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_bf16_kernel<D>, C::kThreads,
+                                                      C::kSmem) != cudaSuccess)
+        return 1;
+    return std::max(1, n);
+}
 
 }  // namespace
 
@@ -414,6 +658,14 @@ int decode_bf16_tile_keys(int head_dim) {
     }
 }
 
+// Pieces are at least min_seg keys long, so a unit of at most `range` keys falls into at
+// most range / min_seg + 2 pieces; min_seg grows with the range so that the count stays
+// near 64 (the scratch layout is sized for it).
+static int min_seg_for(int range, int T) {
+    const int m = std::max(4 * T, (range + 63) / 64);
+    return (m + T - 1) / T * T;
+}
+
 bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
                       int window, int num_sms, DecodePlan *p) {
     int T, occ;
@@ -425,42 +677,33 @@ bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int 
         case 512: T = tile_keys<512>(); occ = ctas_per_sm<512>(); break;
         default: return false;
     }
-    if (occ < 1) occ = 1;
     const int G = n_heads / n_kv_heads;
     const int HB = (G + kHeadsPerBlock - 1) / kHeadsPerBlock;
     const int64_t units = (int64_t)batch * n_kv_heads * HB;
-    const int range = window > 0 ? std::min(max_kv_len, window) : max_kv_len;
-    // The scratch layout depends on the window-free plan only, so a workspace sized by
-    // lat_attn_decode_workspace_size fits every window.
-    auto splits_for = [&](int rng) {
-        const int64_t target = (int64_t)num_sms * occ * 2;  // ~2 CTA waves for balance
-        int64_t sp = (target + units - 1) / std::max<int64_t>(units, 1);
-        sp = std::min<int64_t>(sp, (rng + T - 1) / T);
-        sp = std::min<int64_t>(sp, 512);
-        return (int)std::max<int64_t>(sp, 1);
-    };
-    const int layout_splits = splits_for(std::max(max_kv_len, 1));
-    const int sp = splits_for(std::max(range, 1));
-    int chunk = (std::max(range, 1) + sp - 1) / sp;
-    chunk = (chunk + T - 1) / T * T;
+    // the scratch layout uses the window-free bound, so one workspace fits every window
+    const int layout_range = std::max(max_kv_len, 1);
+    const int min_seg = min_seg_for(layout_range, T);
+    const int layout_splits = (layout_range + min_seg - 1) / min_seg + 2;
     p->head_blocks = HB;
-    p->chunk = chunk;
+    p->min_seg = min_seg;
     p->max_splits = layout_splits;
+    p->grid = num_sms * occ;
     auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
     p->part_o_bytes = round256((size_t)batch * n_heads * layout_splits * head_dim * 4);
     p->part_lse_bytes = round256((size_t)batch * n_heads * layout_splits * 4);
     p->counter_bytes = round256((size_t)units * 4);
     p->total_bytes = p->part_o_bytes + p->part_lse_bytes + p->counter_bytes;
+    (void)window;
     return true;
 }
 
-cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
+cudaError_t launch_decode_bf16(const DecodeArgs &a, int grid, cudaStream_t s) {
     switch (a.head_dim) {
-        case 64: return launch_decode_d<64>(a, s);
-        case 80: return launch_decode_d<80>(a, s);
-        case 128: return launch_decode_d<128>(a, s);
-        case 256: return launch_decode_d<256>(a, s);
-        case 512: return launch_decode_d<512>(a, s);
+        case 64: return launch_decode_d<64>(a, grid, s);
+        case 80: return launch_decode_d<80>(a, grid, s);
+        case 128: return launch_decode_d<128>(a, grid, s);
+        case 256: return launch_decode_d<256>(a, grid, s);
+        case 512: return launch_decode_d<512>(a, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }

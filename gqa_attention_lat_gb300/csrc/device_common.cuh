@@ -49,6 +49,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
                  ::"r"(smem_u32(bar)) : "memory");
 }
 
+// `count` arrivals at once (on behalf of several warps)
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t count) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile(
         "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
@@ -100,8 +106,17 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *desc, ui
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *desc, uint64_t *bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(smem_dst)), "l"(desc), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // ------------------------------------------------------------------------------
-// cp.async (Ampere-style 16-byte copies, used by the decode kernel)
+// cp.async (Ampere-style 16-byte copies)
 
 __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc, bool valid) {
     // src-size 0 reads nothing and fills the 16 bytes with zeros

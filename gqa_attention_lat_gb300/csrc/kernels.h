@@ -44,6 +44,7 @@ cudaError_t launch_row_attention_f32(const RowAttnArgs &a, cudaStream_t s);
 // ---------------------------------------------------------------- bf16 split-KV decode
 struct DecodeArgs {
     CUtensorMap tm_k, tm_v;  // 4-D maps (d, head, row < max_kv_len, sequence), 128-byte swizzle
+    CUtensorMap tm_q;        // 3-D map (d, query head, sequence), 8-head boxes, 128-byte swizzle
     const __nv_bfloat16 *q;
     int64_t q_rs;
     const __nv_bfloat16 *k_cache, *v_cache;
@@ -59,18 +60,19 @@ struct DecodeArgs {
     float *part_o;      // [batch, n_heads, max_splits, head_dim]
     float *part_lse;    // [batch, n_heads, max_splits]
     int32_t *counters;  // [batch, n_kv_heads, head_blocks]
-    int max_splits, chunk;
+    int max_splits;  // partial slots per (sequence, KV head, head block)
+    int min_seg;     // shortest stretch of one unit's keys a CTA takes (multiple of the tile)
     int32_t *status;
 };
 struct DecodePlan {
-    int head_blocks, max_splits, chunk;
+    int head_blocks, max_splits, min_seg, grid;
     size_t part_o_bytes, part_lse_bytes, counter_bytes, total_bytes;
 };
 // Chooses the split size and the scratch layout; false when the shape is not built.
 bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
                       int window, int num_sms, DecodePlan *plan);
 int decode_bf16_tile_keys(int head_dim);     // cache rows per TMA box for this head_dim
-cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode_bf16(const DecodeArgs &a, int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------- bf16 tensor-core prefill
 struct PrefillTcArgs {

@@ -131,8 +131,10 @@ size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int 
  * LAT_ERR_WORKSPACE.  The size depends on the current device's SM count: size the
  * workspace with the device current that will run the call.  LAT_F32 needs no
  * workspace (its size is 0 and the pointer may be NULL).
- * For LAT_BF16, q and the cache base pointers must be 16-byte aligned and q_rs,
- * cache_rs, cache_head_stride, cache_seq_stride multiples of 8.
+ * For LAT_BF16, q, out and the cache base pointers must be 16-byte aligned and q_rs,
+ * out_rs, cache_rs, cache_head_stride, cache_seq_stride multiples of 8 (tiles arrive
+ * through the tensor-memory-access unit and results leave in 16-byte vectors), else
+ * LAT_ERR_INVALID_ARG.
  */
 lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
                            const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,

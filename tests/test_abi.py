@@ -103,6 +103,8 @@ def _decode(**kw):
     (dict(cache_rs=0), binding.LAT_ERR_INVALID_ARG),
     (dict(cache_rs=1020), binding.LAT_ERR_INVALID_ARG),               # bf16 stride % 8
     (dict(k_cache=FAKE + 4), binding.LAT_ERR_INVALID_ARG),
+    (dict(out=FAKE + 8), binding.LAT_ERR_INVALID_ARG),                # bf16 output misaligned
+    (dict(out_rs=4100), binding.LAT_ERR_INVALID_ARG),                 # not a multiple of 8
 ])
 def test_decode_rejects_on_host(lib, kw, code):
     with pytest.raises(binding.LatError) as e:
