@@ -126,6 +126,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     uint64_t *q_full = empty + C::kStages;                                // [2]
     uint64_t *q_empty = q_full + 2;                                       // [2]
     uint64_t *parked = q_empty + 2;                                       // piece states parked
+    uint64_t *merge_bar = parked + 1;                                     // partials staged
     long long *total_p = reinterpret_cast<long long *>(parked + 2);       // key-stream length
     long long *start_p = total_p + 1;                                     // first sequence's offset
     int *start_b = reinterpret_cast<int *>(start_p + 1);                  // CTA's first sequence
@@ -208,6 +209,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
             mbar_init(&q_empty[i], C::kWarps);
         }
         mbar_init(parked, C::kWarps);
+        mbar_init(merge_bar, 1);
         *abort_flag = 0;
         *n_merge = 0;
         fence_mbarrier_init();
@@ -573,49 +575,101 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     }
 
     // ---- merge the units this CTA finished last: lse-weighted sum of their pieces ----
-    // One thread per 4 output elements; every partial it needs is loaded before any is
-    // used, so a merge costs about one round trip to L2.
+    // The partial rows of a head sit side by side in the scratch, so one bulk copy per
+    // head stages all of them in the (now idle) ring: one round trip to L2 per unit.
+    // Meanwhile each warp turns its heads' partial lse values into weights.
     __threadfence();
     const int n_merges = min(*n_merge, kMaxMerges);
+    float *wts = reinterpret_cast<float *>(sQ);  // [g][nseg] weights, then [g] lse
     for (int mi = 0; mi < n_merges; ++mi) {
         const int b = merge_unit[4 * mi + 0], h_base = merge_unit[4 * mi + 1];
         const int g_cnt = merge_unit[4 * mi + 2];
         const int nseg = merge_unit[4 * mi + 3] & 0xff, unit = merge_unit[4 * mi + 3] >> 8;
-        constexpr int kV4 = D / 4;
-        for (int i = tid; i < g_cnt * kV4; i += C::kThreads) {
-            const int g = i / kV4, x = 4 * (i % kV4);
-            const int64_t rb = ((int64_t)b * a.n_heads + h_base + g) * a.max_splits;
-            float M = -INFINITY, Z = 0.f;
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp0 = 0; sp0 < nseg; sp0 += 4) {  // four partials per batch of loads
-                float lv[4];
-                float4 ov[4];
+        const uint32_t row_bytes = (uint32_t)nseg * D * 4;
+        const bool staged = nseg <= 96 &&
+                            (size_t)g_cnt * row_bytes <= (size_t)C::kStages * C::kStageBytes &&
+                            kHeadsPerBlock * (nseg + 1) * 4 <= 2 * C::kQBytes;
+        if (staged && tid == 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(merge_bar, (uint32_t)g_cnt * row_bytes);
+            for (int g = 0; g < g_cnt; ++g)
+                bulk_load(sRing + g * row_bytes,
+                          a.part_o + ((int64_t)b * a.n_heads + h_base + g) * a.max_splits * D,
+                          row_bytes, merge_bar);
+        }
+        if (staged) {
+            for (int g = warp; g < g_cnt; g += C::kWarps + 1) {
+                const int64_t rb = ((int64_t)b * a.n_heads + h_base + g) * a.max_splits;
+                float lv[3];  // nseg <= 96 (the scratch layout keeps it near 66)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const bool in = sp0 + k < nseg;
-                    lv[k] = in ? __ldcg(a.part_lse + rb + sp0 + k) : -INFINITY;
-                    ov[k] = in ? __ldcg(reinterpret_cast<const float4 *>(a.part_o + (rb + sp0 + k) * D + x))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < 3; ++k)
+                    lv[k] = lane + 32 * k < nseg ? __ldcg(a.part_lse + rb + lane + 32 * k) : -INFINITY;
+                float M = fmaxf(fmaxf(lv[0], lv[1]), lv[2]);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                float e[3], Z = 0.f;
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    e[k] = lv[k] == -INFINITY ? 0.f : fast_exp2(lv[k] - M);
+                    Z += e[k];
                 }
-                float mb = M;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mb = fmaxf(mb, lv[k]);
-                const float c = M == -INFINITY ? 0.f : fast_exp2(M - mb);  // rescale earlier batches
-                Z *= c;
-                o.x *= c; o.y *= c; o.z *= c; o.w *= c;
+                for (int off = 16; off > 0; off >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, off);
+                const float rz = 1.f / Z;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float e = lv[k] == -INFINITY ? 0.f : fast_exp2(lv[k] - mb);
-                    Z += e;
-                    o.x += e * ov[k].x; o.y += e * ov[k].y; o.z += e * ov[k].z; o.w += e * ov[k].w;
-                }
-                M = mb;
+                for (int k = 0; k < 3; ++k)
+                    if (lane + 32 * k < nseg) wts[g * nseg + lane + 32 * k] = e[k] * rz;
+                if (lane == 0) wts[kHeadsPerBlock * nseg + g] = M + log2f(Z);
             }
-            const float rz = 1.f / Z;
-            *reinterpret_cast<uint2 *>(a.out + (int64_t)b * a.out_rs + (int64_t)(h_base + g) * D + x) =
-                make_uint2(pack_bf16x2(o.x * rz, o.y * rz), pack_bf16x2(o.z * rz, o.w * rz));
-            if (x == 0 && a.lse != nullptr)
-                a.lse[(int64_t)b * a.n_heads + h_base + g] = (M + log2f(Z)) * kLn2;
+            __syncthreads();
+            const bool got = mbar_wait_bounded(merge_bar, mi & 1, abort_flag, deadline);
+            if (!__syncthreads_and(got)) {  // the copies must land before the CTA may go
+                volatile int no_abort = 0;
+                mbar_wait_bounded(merge_bar, mi & 1, &no_abort, globaltimer_ns() + 100000000ull);
+                if (tid == 0) report_status(a.status, kErrTimeout);
+                return;
+            }
+            constexpr int kV4 = D / 4;
+            for (int i = tid; i < g_cnt * kV4; i += C::kThreads) {
+                const int g = i / kV4, x = 4 * (i % kV4);
+                const float *src = reinterpret_cast<const float *>(sRing + g * row_bytes) + x;
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sp = 0; sp < nseg; ++sp) {
+                    const float w = wts[g * nseg + sp];
+                    const float4 v = *reinterpret_cast<const float4 *>(src + sp * D);
+                    o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+                }
+                *reinterpret_cast<uint2 *>(a.out + (int64_t)b * a.out_rs + (int64_t)(h_base + g) * D + x) =
+                    make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+                if (x == 0 && a.lse != nullptr)
+                    a.lse[(int64_t)b * a.n_heads + h_base + g] = wts[kHeadsPerBlock * nseg + g] * kLn2;
+            }
+            __syncthreads();  // the ring and weights are reused by the next unit
+        } else {
+            // too many pieces to stage: one thread per 4 outputs, partials straight from L2
+            constexpr int kV4 = D / 4;
+            for (int i = tid; i < g_cnt * kV4; i += C::kThreads) {
+                const int g = i / kV4, x = 4 * (i % kV4);
+                const int64_t rb = ((int64_t)b * a.n_heads + h_base + g) * a.max_splits;
+                float M = -INFINITY, Z = 0.f;
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sp = 0; sp < nseg; ++sp) {
+                    const float l = __ldcg(a.part_lse + rb + sp);
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (rb + sp) * D + x));
+                    const float mn = fmaxf(M, l);
+                    const float c = M == -INFINITY ? 0.f : fast_exp2(M - mn);
+                    const float e = fast_exp2(l - mn);
+                    Z = Z * c + e;
+                    o.x = o.x * c + e * v.x; o.y = o.y * c + e * v.y;
+                    o.z = o.z * c + e * v.z; o.w = o.w * c + e * v.w;
+                    M = mn;
+                }
+                const float rz = 1.f / Z;
+                *reinterpret_cast<uint2 *>(a.out + (int64_t)b * a.out_rs + (int64_t)(h_base + g) * D + x) =
+                    make_uint2(pack_bf16x2(o.x * rz, o.y * rz), pack_bf16x2(o.z * rz, o.w * rz));
+                if (x == 0 && a.lse != nullptr)
+                    a.lse[(int64_t)b * a.n_heads + h_base + g] = (M + log2f(Z)) * kLn2;
+            }
         }
         if (tid == 0) a.counters[unit] = 0;  // ready for the next call
     }

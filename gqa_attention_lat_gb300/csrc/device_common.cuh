@@ -106,6 +106,21 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *desc, ui
         : "memory");
 }
 
+// contiguous global -> shared copy of `bytes` (multiple of 16, both ends 16-byte aligned)
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// order earlier generic-proxy global accesses (seen through an acquire) before later
+// async-proxy (bulk copy) reads of global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *desc, uint64_t *bar,
                                             int c0, int c1, int c2) {
     asm volatile(

@@ -29,6 +29,10 @@ SWEEP = [
     (2, 16, 1, 128, 300, [300, 77], 0, "bf16"),           # G = 16: two head blocks
     (3, 4, 2, 512, 2000, [2000, 1500, 1], 0, "bf16"),
     (2, 8, 8, 64, 64, [64, 5], 0, "bf16"),                # G = 1
+    # one long sequence cut into many pieces: about 20 (merged from a shared-memory copy
+    # of the partials) and about 64 (too many to stage: merged straight from L2)
+    (1, 8, 1, 128, 5000, [5000], 0, "bf16"),
+    (1, 8, 1, 512, 32768, [32768], 0, "bf16"),
     # sliding window: the visible keys start at a non-zero cache offset
     (4, 8, 2, 128, 3000, [3000, 1024, 1025, 40], 1024, "bf16"),
     (2, 8, 4, 256, 500, [500, 18], 17, "bf16"),
