@@ -9,8 +9,11 @@
 //
 // How (GB300 design; the pages' Metal kernels are prior art only):
 //  * One CTA owns a 128-row query tile of one head (one TMEM lane per query row).
-//  * Warp roles: warps 0-3 run the softmax (thread t <-> query row t), warp 4 issues TMA
-//    loads, warp 5 issues tcgen05.mma.  Synchronisation is by mbarriers only.
+//  * Warp roles: warps 0-7 run the softmax as two warpgroups that split each S tile's
+//    columns (thread t of a warpgroup <-> query row t; the two halves meet through a
+//    small shared-memory exchange for the row max and sum), warp 8 loads Q and K tiles
+//    with TMA, warp 9 loads V tiles, warp 10 issues tcgen05.mma.  Synchronisation is by
+//    mbarriers only.
 //  * S = Q K^T is accumulated in tensor memory (fp32, double-buffered so the MMA of tile
 //    j+1 overlaps the softmax of tile j); P = exp2(S*scale*log2e - m) is written as bf16
 //    back into the S buffer it came from, and O += P V reads it straight from tensor
