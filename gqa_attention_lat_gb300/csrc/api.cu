@@ -173,7 +173,9 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
     a.status = status;
     a.timeout_ns = timeout_ns;
     a.test_skip_kv_load = skip_kv_load;
-    return lat::launch_prefill_tc(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
+    int sms = 0;
+    if (!current_sm_count(&sms)) return LAT_ERR_CUDA;
+    return lat::launch_prefill_tc(a, sms, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
 }
 
 }  // namespace

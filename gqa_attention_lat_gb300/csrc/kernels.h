@@ -87,6 +87,6 @@ struct PrefillTcArgs {
     int test_skip_kv_load;         // test hook: never load KV tile 0 (forces a timeout)
 };
 int prefill_tc_block_n(int head_dim);        // keys per KV tile for this head_dim
-cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace lat

@@ -37,6 +37,8 @@
 //    LAT_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees tensor memory and exits.
 #include <math.h>
 
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -70,9 +72,10 @@ struct TcCfg {
     static constexpr int kKStages = D == 64 ? 4 : (D <= 128 ? 3 : 1);
     static constexpr int kVStages = D == 64 ? 4 : (D <= 128 ? 2 : 1);
     static constexpr int kQBytes = kQkChunks * kBM * 128;
+    static constexpr int kQStages = D <= 128 ? 2 : 1;   // the next item's Q loads early
     static constexpr int kBarBytes = 256 + 4 * kBM * 4;  // barriers + row exchange
-    static constexpr int kPayload = kQBytes + kKStages * kKTileBytes + kVStages * kVTileBytes +
-                                    kBarBytes;
+    static constexpr int kPayload = kQStages * kQBytes + kKStages * kKTileBytes +
+                                    kVStages * kVTileBytes + kBarBytes;
     // 1 KB of slack lets the 1024-byte aligned carve-up start anywhere; a shape that
     // cannot afford it relies on the dynamic shared memory base being 1024-byte aligned
     // (checked at run time)
@@ -138,6 +141,41 @@ __device__ __forceinline__ Band kv_band(int m0, int rows, int S, int L, int caus
     return b;
 }
 
+// One unit of work: a 128-row query tile of one query head (and one O half for D = 512).
+struct Item {
+    int b, h, half, m0, rows, hk;
+    Band band;
+};
+
+// Items are numbered heaviest first (latest query tiles, which see the most keys under a
+// causal mask), then by sequence and head.
+template <int D>
+__device__ __forceinline__ Item item_at(const PrefillTcArgs &a, int idx) {
+    using C = TcCfg<D>;
+    const int per_tile = a.batch * a.n_heads * C::kSplitO;
+    const int n_mtiles = (a.seq_len + kBM - 1) / kBM;
+    const int z = idx / per_tile, rem = idx % per_tile;
+    const int mt = n_mtiles - 1 - z;
+    Item it;
+    it.b = rem / (a.n_heads * C::kSplitO);
+    const int head_sel = rem % (a.n_heads * C::kSplitO);
+    it.h = head_sel / C::kSplitO;
+    it.half = head_sel % C::kSplitO;
+    it.m0 = mt * kBM;
+    it.rows = min(kBM, a.seq_len - it.m0);
+    it.hk = it.h / (a.n_heads / a.n_kv_heads);
+    it.band = kv_band(it.m0, it.rows, a.seq_len, a.kv_len, a.causal, a.window, C::kBN);
+    return it;
+}
+
+// The k-th item of CTA c in a grid of G: rounds of G items in heaviest-first order, dealt
+// forwards and backwards in turn (a "snake"), so that the CTA with the heaviest item of
+// one round gets the lightest of the next.  -1 past the end.
+__device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
+    const int idx = k * G + ((k & 1) ? G - 1 - c : c);
+    return idx < n_items ? idx : -1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
@@ -150,17 +188,19 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         if (threadIdx.x == 0) report_status(a.status, kErrCuda);
         return;
     }
-    unsigned char *sQ = smem;
-    unsigned char *sK = sQ + C::kQBytes;                      // [kKStages] K tiles
+    unsigned char *sQ = smem;                                 // [kQStages] Q tiles
+    unsigned char *sK = sQ + C::kQStages * C::kQBytes;        // [kKStages] K tiles
     unsigned char *sV = sK + C::kKStages * C::kKTileBytes;    // [kVStages] V tiles
     uint64_t *bars = reinterpret_cast<uint64_t *>(sV + C::kVStages * C::kVTileBytes);
-    uint64_t *bar_q = bars + 0;
-    uint64_t *bar_s = bars + 1;        // [2]
-    uint64_t *bar_p = bars + 3;        // [2] P(t) ready, alternating by tile parity
-    uint64_t *bar_o = bars + 5;
-    uint64_t *bar_done = bars + 6;     // every MMA complete (drain and epilogue)
-    uint64_t *bar_x = bars + 7;        // [4] softmax row exchange, one per TMEM lane quarter
-    uint64_t *k_full = bars + 11;      // [kKStages]
+    uint64_t *q_full = bars + 0;       // [2]
+    uint64_t *q_empty = bars + 2;      // [2]
+    uint64_t *bar_s = bars + 4;        // [2] S(g) ready, by global tile parity
+    uint64_t *bar_p = bars + 6;        // [2] P(g) ready
+    uint64_t *bar_o = bars + 8;        // one phase per P.V MMA group (global tile order)
+    uint64_t *o_full = bars + 9;       // one phase per item: its O is complete
+    uint64_t *bar_done = bars + 10;    // every MMA complete (drain)
+    uint64_t *bar_x = bars + 11;       // [4] softmax row exchange, one per TMEM lane quarter
+    uint64_t *k_full = bars + 15;      // [kKStages]
     uint64_t *k_empty = k_full + C::kKStages;
     uint64_t *v_full = k_empty + C::kKStages;   // [kVStages]
     uint64_t *v_empty = v_full + C::kVStages;
@@ -169,28 +209,20 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     float *xchg = reinterpret_cast<float *>(bars + 32);   // [2 parities][2 warpgroups][kBM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int head_sel = blockIdx.x;               // h * kSplitO + half
-    const int h = head_sel / C::kSplitO;
-    const int half = head_sel % C::kSplitO;
-    const int b = blockIdx.y;
-    const int n_mtiles = (a.seq_len + kBM - 1) / kBM;
-    const int mt = n_mtiles - 1 - (int)blockIdx.z;  // heaviest (latest) query tiles first
-    const int m0 = mt * kBM;
-    const int rows = min(kBM, a.seq_len - m0);
-    const int hk = h / (a.n_heads / a.n_kv_heads);
-    const int v_col0 = half * C::kOCols;
-    const Band band = kv_band(m0, rows, a.seq_len, a.kv_len, a.causal, a.window, BN);
-    const int n_tiles = band.t_end - band.t_begin;
+    const int n_items = a.batch * a.n_heads * C::kSplitO * ((a.seq_len + kBM - 1) / kBM);
+    const int cta = blockIdx.x, G = gridDim.x;
     const uint64_t deadline = globaltimer_ns() + a.timeout_ns;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar_q, 1);
-        mbar_init(&bar_s[0], 1);
-        mbar_init(&bar_s[1], 1);
-        mbar_init(&bar_p[0], kSoftmaxThreads);
-        mbar_init(&bar_p[1], kSoftmaxThreads);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+            mbar_init(&bar_s[i], 1);
+            mbar_init(&bar_p[i], kSoftmaxThreads);
+        }
         for (int q = 0; q < 4; ++q) mbar_init(&bar_x[q], 2);  // one arrival per warp
         mbar_init(bar_o, 1);
+        mbar_init(o_full, 1);
         mbar_init(bar_done, 1);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&k_full[s], 1);
@@ -214,8 +246,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
 
     if (warp == kKProducerWarp || warp == kVProducerWarp) {
         // ------------------------------------------------------------ TMA producers
-        // warp 8 loads Q, then every K tile; warp 9 loads every V tile (this CTA's O
-        // columns).  One mbarrier per tile carries all of the tile's chunk copies.
+        // warp 8 loads each item's Q, then its K tiles; warp 9 loads its V tiles (this
+        // item's O columns).  The rings run on across items.  One mbarrier per tile
+        // carries all of the tile's chunk copies.
         if (lane == 0) {
             const bool is_k = warp == kKProducerWarp;
             const int stages = is_k ? C::kKStages : C::kVStages;
@@ -225,95 +258,140 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             uint64_t *full = is_k ? k_full : v_full;
             uint64_t *empty = is_k ? k_empty : v_empty;
             const CUtensorMap *tm = is_k ? &a.tm_k : &a.tm_v;
-            const int col0 = is_k ? 0 : v_col0;
             tma_prefetch_desc(tm);
-            if (is_k) {
-                tma_prefetch_desc(&a.tm_q);
-                mbar_arrive_expect_tx(bar_q, C::kQBytes);
-                for (int c = 0; c < C::kQkChunks; ++c)
-                    tma_load_4d(sQ + c * kBM * 128, &a.tm_q, bar_q, c * kChunkCols, h, m0, b);
+            if (is_k) tma_prefetch_desc(&a.tm_q);
+            int g = 0, qi = 0;  // tiles and query tiles issued
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int idx = item_index(k, cta, G, n_items);
+                if (idx < 0) break;
+                const Item it = item_at<D>(a, idx);
+                if (is_k) {
+                    const int qs = qi % C::kQStages;
+                    if (!mbar_wait_bounded(&q_empty[qs], ((qi / C::kQStages) & 1) ^ 1, abort_flag,
+                                           deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
+                    for (int c = 0; c < C::kQkChunks; ++c)
+                        tma_load_4d(sQ + qs * C::kQBytes + c * kBM * 128, &a.tm_q, &q_full[qs],
+                                    c * kChunkCols, it.h, it.m0, it.b);
+                    ++qi;
+                }
+                const int col0 = is_k ? 0 : it.half * C::kOCols;
+                for (int t = it.band.t_begin; t < it.band.t_end; ++t, ++g) {
+                    const int s = g % stages;
+                    if (!mbar_wait_bounded(&empty[s], ((g / stages) & 1) ^ 1, abort_flag, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    if (is_k && a.test_skip_kv_load && g == 0) continue;  // test hook: never load
+                    mbar_arrive_expect_tx(&full[s], tile_bytes);
+                    for (int c = 0; c < chunks; ++c)
+                        tma_load_4d(ring + s * tile_bytes + c * C::kChunkBytes, tm, &full[s],
+                                    col0 + c * kChunkCols, it.hk, t * BN, it.b);
+                }
             }
-            int last_issued[4] = {-1, -1, -1, -1};  // per stage: tile index of its last load
-            for (int t = 0; t < n_tiles; ++t) {
-                const int s = t % stages;
-                if (!mbar_wait_bounded(&empty[s], ((t / stages) & 1) ^ 1, abort_flag, deadline))
-                    break;
-                if (is_k && a.test_skip_kv_load && t == 0) continue;  // test hook: never load
-                mbar_arrive_expect_tx(&full[s], tile_bytes);
-                const int key0 = (band.t_begin + t) * BN;
-                for (int c = 0; c < chunks; ++c)
-                    tma_load_4d(ring + s * tile_bytes + c * C::kChunkBytes, tm, &full[s],
-                                col0 + c * kChunkCols, hk, key0, b);
-                last_issued[s] = t;
-            }
-            // drain: every issued copy must land before the CTA may exit
+            // drain: every issued copy must land before the CTA may exit.  Fills go round
+            // each ring in order, so slot s last held fill s + j*stages, the largest below
+            // the count issued.
             const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
             volatile int no_abort = 0;
-            if (is_k) mbar_wait_bounded(bar_q, 0, &no_abort, drain_deadline);
             for (int s = 0; s < stages; ++s)
-                if (last_issued[s] >= 0)
-                    mbar_wait_bounded(&full[s], (last_issued[s] / stages) & 1, &no_abort,
-                                      drain_deadline);
+                if (s < g) {
+                    const int last = s + (g - 1 - s) / stages * stages;
+                    if (!(is_k && a.test_skip_kv_load && last == 0))
+                        mbar_wait_bounded(&full[s], (last / stages) & 1, &no_abort, drain_deadline);
+                }
+            if (is_k)
+                for (int s = 0; s < C::kQStages; ++s)
+                    if (s < qi) {
+                        const int last = s + (qi - 1 - s) / C::kQStages * C::kQStages;
+                        mbar_wait_bounded(&q_full[s], (last / C::kQStages) & 1, &no_abort,
+                                          drain_deadline);
+                    }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = instr_desc(kBM, BN, false);
+            constexpr uint32_t idesc_pv = instr_desc(kBM, C::kOCols, true);
             // Descriptors are built once; advancing an operand by B bytes adds B >> 4 to
             // the start-address field (all smem addresses here are below 256 KB, so the
             // 14-bit field never carries), which keeps the issue loop to a few
             // instructions per MMA.
             const uint64_t dq0 = sw128_desc(smem_u32(sQ));
             const uint64_t dk0 = sw128_desc(smem_u32(sK));
-            bool ok = mbar_wait_bounded(bar_q, 0, abort_flag, deadline);
-            tc_fence_after();
-            for (int t = 0; t <= n_tiles && ok; ++t) {
-                if (t < n_tiles) {
-                    // S(t) = Q K(t)^T into S buffer t % 2
-                    const int s = t % C::kKStages;
-                    if (!mbar_wait_bounded(&k_full[s], (t / C::kKStages) & 1, abort_flag, deadline)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_s = tmem + kTmemS + (uint32_t)((t & 1) * BN);
-                    const uint64_t dk = dk0 + (uint64_t)((s * C::kKTileBytes) >> 4);
-#pragma unroll
-                    for (int c = 0; c < C::kQkChunks; ++c) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            if (c * 4 + kk < C::kKSteps)
-                                tc_mma_ss(d_s, dq0 + (uint64_t)((c * kBM * 128 + kk * 32) >> 4),
-                                          dk + (uint64_t)((c * C::kChunkBytes + kk * 32) >> 4),
-                                          idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+            bool ok = true;
+            int g = 0;  // global tile index: S buffer g % 2, ring slots, barrier phases
+            for (int k = 0, qi = 0; ok; ++k, ++qi) {
+                const int idx = item_index(k, cta, G, n_items);
+                if (idx < 0) break;
+                const Item it = item_at<D>(a, idx);
+                const int n_tiles = it.band.t_end - it.band.t_begin;
+                const int qs = qi % C::kQStages;
+                if (!mbar_wait_bounded(&q_full[qs], (qi / C::kQStages) & 1, abort_flag, deadline)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t dq = dq0 + (uint64_t)((qs * C::kQBytes) >> 4);
+                for (int t = 0; t <= n_tiles && ok; ++t) {
+                    if (t < n_tiles) {
+                        // S(g+t) = Q K^T into S buffer (g+t) % 2
+                        const int gt = g + t;
+                        const int s = gt % C::kKStages;
+                        if (!mbar_wait_bounded(&k_full[s], (gt / C::kKStages) & 1, abort_flag, deadline)) {
+                            ok = false;
+                            break;
                         }
-                    }
-                    tc_commit(&k_empty[s]);
-                    tc_commit(&bar_s[t & 1]);
-                }
-                if (t > 0) {
-                    // O += P(t-1) V(t-1): A = P from tensor memory (the S buffer it was
-                    // computed from, 8 columns per 16 keys), B = V MN-major with its 64-column
-                    // atoms kChunkBytes apart, N = every O column of this CTA
-                    const int tp = t - 1;
-                    const int s = tp % C::kVStages;
-                    if (!mbar_wait_bounded(&bar_p[tp & 1], (tp >> 1) & 1, abort_flag, deadline) ||
-                        !mbar_wait_bounded(&v_full[s], (tp / C::kVStages) & 1, abort_flag, deadline)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t dv = sw128_desc_mn(smem_u32(sV) + s * C::kVTileBytes, C::kChunkBytes);
-                    const uint32_t p_tmem = tmem + kTmemS + (uint32_t)((tp & 1) * BN);
-                    constexpr uint32_t idesc_pv = instr_desc(kBM, C::kOCols, true);
+                        tc_fence_after();
+                        const uint32_t d_s = tmem + kTmemS + (uint32_t)((gt & 1) * BN);
+                        const uint64_t dk = dk0 + (uint64_t)((s * C::kKTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        tc_mma_ts(tmem + kTmemO, p_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
-                                  idesc_pv, (tp > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&v_empty[s]);
-                    tc_commit(bar_o);
+                        for (int c = 0; c < C::kQkChunks; ++c) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                if (c * 4 + kk < C::kKSteps)
+                                    tc_mma_ss(d_s, dq + (uint64_t)((c * kBM * 128 + kk * 32) >> 4),
+                                              dk + (uint64_t)((c * C::kChunkBytes + kk * 32) >> 4),
+                                              idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        tc_commit(&k_empty[s]);
+                        tc_commit(&bar_s[gt & 1]);
+                        if (t == n_tiles - 1) tc_commit(&q_empty[qs]);  // Q read for the last time
+                    }
+                    if (t > 0) {
+                        // O += P V for tile g+t-1: A = P from tensor memory (the S buffer it
+                        // was computed from, 8 columns per 16 keys), B = V MN-major with its
+                        // 64-column atoms kChunkBytes apart, N = every O column of the item.
+                        // The first group overwrites O: the previous item's epilogue read it
+                        // before its softmax published this item's first P.
+                        const int gp = g + t - 1;
+                        const int s = gp % C::kVStages;
+                        if (!mbar_wait_bounded(&bar_p[gp & 1], (gp >> 1) & 1, abort_flag, deadline) ||
+                            !mbar_wait_bounded(&v_full[s], (gp / C::kVStages) & 1, abort_flag, deadline)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t dv = sw128_desc_mn(smem_u32(sV) + s * C::kVTileBytes, C::kChunkBytes);
+                        const uint32_t p_tmem = tmem + kTmemS + (uint32_t)((gp & 1) * BN);
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            tc_mma_ts(tmem + kTmemO, p_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
+                                      idesc_pv, (t > 1 || kk > 0) ? 1u : 0u);
+                        tc_commit(&v_empty[s]);
+                        tc_commit(bar_o);
+                    }
                 }
+                if (!ok) break;
+                if (n_tiles == 0) tc_commit(&q_empty[qs]);  // nothing read this Q
+                tc_commit(o_full);  // the item's O is complete once every MMA above is
+                g += n_tiles;
             }
             // drain: all issued MMAs must finish before tensor memory is freed
             tc_commit(bar_done);
@@ -331,24 +409,21 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         const int wg = warp >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
-        const int i = m0 + row;                       // query row within the sequence
-        const int p = i + (a.kv_len - a.seq_len);     // its absolute position
         const int col0 = wg * HC;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const float sl2 = a.scale_log2;
         const bool max_mode = sl2 >= 0.f;             // a negative scale flips max and min
         const float hide = max_mode ? -INFINITY : INFINITY;  // raw value that never wins
-        float m_ref = -INFINITY;  // reference maximum (log2 domain, scaled)
-        float l_part = 0.f;       // this warpgroup's share of the row sum
         bool ok = true;
+        int xn = 0;  // exchanges done (selects the exchange buffer and barrier phase)
         // tcgen05.ld/st are warp-collective, so a wait's outcome is made warp-uniform
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
             const bool r = mbar_wait_bounded(bar, parity, abort_flag, deadline);
             return __all_sync(0xffffffffu, r) != 0;
         };
-        // publish v for the partner warp and read the partner's value (use n of the
-        // exchange barrier of this lane quarter)
-        auto exchange = [&](float v, int n, float &other) {
+        // publish v for the partner warp and read the partner's value
+        auto exchange = [&](float v, float &other) {
+            const int n = xn++;
             xchg[((n & 1) * 2 + wg) * kBM + row] = v;
             __threadfence_block();
             __syncwarp();
@@ -357,116 +432,127 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             other = xchg[((n & 1) * 2 + (wg ^ 1)) * kBM + row];
             return true;
         };
-        for (int t = 0; t < n_tiles; ++t) {
-            if (!wait_warp(&bar_s[t & 1], (t >> 1) & 1)) { ok = false; break; }
-            tc_fence_after();
-            float sv[HC];
-#pragma unroll
-            for (int c = 0; c < HC; c += 16)
-                tmem_ld16(lane_base + kTmemS + (t & 1) * BN + col0 + c,
-                          reinterpret_cast<uint32_t *>(sv + c));
-            tc_wait_ld();
-
-            const int key0 = (band.t_begin + t) * BN;
-            const int p_min = m0 + (a.kv_len - a.seq_len);
-            const bool need_mask = (key0 + BN > a.kv_len) || (a.causal && key0 + BN - 1 > p_min) ||
-                                   (a.window > 0 && key0 < p_min + rows - 1 - a.window + 1);
-            // visible columns of this thread's half: [vlo, vhi)
-            int vlo = 0, vhi = HC;
-            if (need_mask) {
-                const int kc0 = key0 + col0;
-                int jhi = a.kv_len;
-                if (a.causal) jhi = min(jhi, p + 1);
-                vhi = max(0, min(HC, jhi - kc0));
-                if (a.window > 0) vlo = min(HC, max(0, p - a.window + 1 - kc0));
-#pragma unroll
-                for (int c = 0; c < HC; ++c)
-                    if (c < vlo || c >= vhi) sv[c] = hide;
-            }
-            float e[4] = {hide, hide, hide, hide};
-            if (max_mode) {
-#pragma unroll
-                for (int c = 0; c < HC; ++c) e[c & 3] = fmaxf(e[c & 3], sv[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < HC; ++c) e[c & 3] = fminf(e[c & 3], sv[c]);
-            }
-            const float ext = max_mode ? fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]))
-                                       : fminf(fminf(e[0], e[1]), fminf(e[2], e[3]));
-            const float mx_part = vhi > vlo ? ext * sl2 : -INFINITY;
-            float mx_other;
-            if (!exchange(mx_part, t, mx_other)) { ok = false; break; }
-            const float mx = fmaxf(mx_part, mx_other);
-
-            // refresh the reference maximum only when it grew by more than the threshold
-            const bool refresh = mx > m_ref + kRescaleThreshold;
-            const float m_new = refresh ? mx : m_ref;
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;  // no key seen yet
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-            if (need_mask) {
-#pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    const float w = fast_exp2(fmaf(sv[c], sl2, -m_use));
-                    sv[c] = (c >= vlo && c < vhi) ? w : 0.f;
-                    rs[c & 3] += sv[c];
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    sv[c] = fast_exp2(fmaf(sv[c], sl2, -m_use));
-                    rs[c & 3] += sv[c];
-                }
-            }
-            const float corr = refresh ? fast_exp2(m_ref - m_use) : 1.f;  // 0 when m_ref = -inf
-
-            // this half of P (bf16 pairs) into the S buffer it came from: both warpgroups
-            // have read their S columns (the exchange above orders that), and P(t) sits
-            // where PV(t) will read it
-            {
-                const uint32_t pcol = lane_base + kTmemS + (t & 1) * BN + col0 / 2;
-#pragma unroll
-                for (int c = 0; c < HC / 2; c += 8) {
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(sv[2 * (c + k)], sv[2 * (c + k) + 1]);
-                    tmem_st8(pcol + c, pk);
-                }
-            }
-            // rescale this warpgroup's O chunks when any row of the warp refreshed; O is
-            // stable once PV(t-1) completes (the S(t) commit already covered PV(t-2), so
-            // phase t-1 of bar_o is the next one to complete)
-            if (t > 0 && __any_sync(0xffffffffu, refresh)) {
-                if (!wait_warp(bar_o, (t - 1) & 1)) { ok = false; break; }
+        int g = 0;  // global tile index
+        for (int k = 0; ok; ++k) {
+            const int idx = item_index(k, cta, G, n_items);
+            if (idx < 0) break;
+            const Item it = item_at<D>(a, idx);
+            const int n_tiles = it.band.t_end - it.band.t_begin;
+            const int i = it.m0 + row;                       // query row within the sequence
+            const int p = i + (a.kv_len - a.seq_len);        // its absolute position
+            const int p_min = it.m0 + (a.kv_len - a.seq_len);
+            float m_ref = -INFINITY;  // reference maximum (log2 domain, scaled)
+            float l_part = 0.f;       // this warpgroup's share of the row sum
+            for (int t = 0; t < n_tiles; ++t) {
+                const int gt = g + t;
+                if (!wait_warp(&bar_s[gt & 1], (gt >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 16 * wg; c < C::kOCols; c += 32) {
-                    uint32_t ov[16];
-                    tmem_ld16(lane_base + kTmemO + c, ov);
-                    tc_wait_ld();
+                float sv[HC];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        ov[k] = __float_as_uint(__uint_as_float(ov[k]) * corr);
-                    tmem_st16(lane_base + kTmemO + c, ov);
+                for (int c = 0; c < HC; c += 16)
+                    tmem_ld16(lane_base + kTmemS + (gt & 1) * BN + col0 + c,
+                              reinterpret_cast<uint32_t *>(sv + c));
+                tc_wait_ld();
+
+                const int key0 = (it.band.t_begin + t) * BN;
+                const bool need_mask = (key0 + BN > a.kv_len) || (a.causal && key0 + BN - 1 > p_min) ||
+                                       (a.window > 0 && key0 < p_min + it.rows - 1 - a.window + 1);
+                // visible columns of this thread's half: [vlo, vhi)
+                int vlo = 0, vhi = HC;
+                if (need_mask) {
+                    const int kc0 = key0 + col0;
+                    int jhi = a.kv_len;
+                    if (a.causal) jhi = min(jhi, p + 1);
+                    vhi = max(0, min(HC, jhi - kc0));
+                    if (a.window > 0) vlo = min(HC, max(0, p - a.window + 1 - kc0));
+#pragma unroll
+                    for (int c = 0; c < HC; ++c)
+                        if (c < vlo || c >= vhi) sv[c] = hide;
                 }
+                float e[4] = {hide, hide, hide, hide};
+                if (max_mode) {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) e[c & 3] = fmaxf(e[c & 3], sv[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) e[c & 3] = fminf(e[c & 3], sv[c]);
+                }
+                const float ext = max_mode ? fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]))
+                                           : fminf(fminf(e[0], e[1]), fminf(e[2], e[3]));
+                const float mx_part = vhi > vlo ? ext * sl2 : -INFINITY;
+                float mx_other;
+                if (!exchange(mx_part, mx_other)) { ok = false; break; }
+                const float mx = fmaxf(mx_part, mx_other);
+
+                // refresh the reference maximum only when it grew by more than the threshold
+                const bool refresh = mx > m_ref + kRescaleThreshold;
+                const float m_new = refresh ? mx : m_ref;
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;  // no key seen yet
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) {
+                        const float w = fast_exp2(fmaf(sv[c], sl2, -m_use));
+                        sv[c] = (c >= vlo && c < vhi) ? w : 0.f;
+                        rs[c & 3] += sv[c];
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) {
+                        sv[c] = fast_exp2(fmaf(sv[c], sl2, -m_use));
+                        rs[c & 3] += sv[c];
+                    }
+                }
+                const float corr = refresh ? fast_exp2(m_ref - m_use) : 1.f;  // 0 when m_ref = -inf
+
+                // this half of P (bf16 pairs) into the S buffer it came from: both
+                // warpgroups have read their S columns (the exchange above orders that),
+                // and P sits where its P.V MMA will read it
+                {
+                    const uint32_t pcol = lane_base + kTmemS + (gt & 1) * BN + col0 / 2;
+#pragma unroll
+                    for (int c = 0; c < HC / 2; c += 8) {
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            pk[kk] = pack_bf16x2(sv[2 * (c + kk)], sv[2 * (c + kk) + 1]);
+                        tmem_st8(pcol + c, pk);
+                    }
+                }
+                // rescale this warpgroup's O chunks when any row of the warp refreshed; O
+                // is stable once the previous tile's P.V completes (the S commit of this
+                // tile already covered the one before, so that is the next phase of bar_o)
+                if (t > 0 && __any_sync(0xffffffffu, refresh)) {
+                    if (!wait_warp(bar_o, (gt - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 16 * wg; c < C::kOCols; c += 32) {
+                        uint32_t ov[16];
+                        tmem_ld16(lane_base + kTmemO + c, ov);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk)
+                            ov[kk] = __float_as_uint(__uint_as_float(ov[kk]) * corr);
+                        tmem_st16(lane_base + kTmemO + c, ov);
+                    }
+                }
+                tc_wait_st();
+                l_part = l_part * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+                m_ref = m_new;
+                tc_fence_before();
+                mbar_arrive(&bar_p[gt & 1]);
             }
-            tc_wait_st();
-            l_part = l_part * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-            m_ref = m_new;
-            tc_fence_before();
-            mbar_arrive(&bar_p[t & 1]);
-        }
-        // ---- epilogue: O / l -> bf16 rows, lse -----------------------------------
-        if (ok && n_tiles > 0) {
-            ok = wait_warp(bar_done, 0);
+            if (!ok) break;
+            g += n_tiles;
+            // ---- epilogue of the item: O / l -> bf16 rows, lse ---------------------------
+            if (!wait_warp(o_full, k & 1)) { ok = false; break; }
             tc_fence_after();
-        }
-        float l_other = 0.f;
-        if (ok) ok = exchange(l_part, n_tiles, l_other);
-        if (ok) {
+            float l_other = 0.f;
+            if (!exchange(l_part, l_other)) { ok = false; break; }
             const float l_sum = l_part + l_other;
-            const bool live = row < rows;  // rows past the sequence end are not stored
-            const int64_t qrow = (int64_t)b * a.seq_len + i;
-            __nv_bfloat16 *orow = a.out + qrow * a.out_rs + (int64_t)h * D + v_col0;
+            const bool live = row < it.rows;  // rows past the sequence end are not stored
+            const int64_t qrow = (int64_t)it.b * a.seq_len + i;
+            __nv_bfloat16 *orow = a.out + qrow * a.out_rs + (int64_t)it.h * D + it.half * C::kOCols;
             const bool empty = !(l_sum > 0.f);
             const float inv_l = empty ? 0.f : 1.f / l_sum;
             if (n_tiles > 0) {
@@ -477,9 +563,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     tc_wait_ld();
                     uint32_t pk[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        pk[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv_l,
-                                            __uint_as_float(ov[2 * k + 1]) * inv_l);
+                    for (int kk = 0; kk < 8; ++kk)
+                        pk[kk] = pack_bf16x2(__uint_as_float(ov[2 * kk]) * inv_l,
+                                             __uint_as_float(ov[2 * kk + 1]) * inv_l);
                     if (live) {
                         uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
                         dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -488,11 +574,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                 }
             } else if (live) {
                 for (int c = 16 * wg; c < C::kOCols; c += 32)
-                    for (int k = 0; k < 16; ++k) orow[c + k] = __float2bfloat16_rn(0.f);
+                    for (int kk = 0; kk < 16; ++kk) orow[c + kk] = __float2bfloat16_rn(0.f);
             }
-            if (live && wg == 0 && a.lse != nullptr && half == 0)
-                a.lse[qrow * a.n_heads + h] =
+            if (live && wg == 0 && a.lse != nullptr && it.half == 0)
+                a.lse[qrow * a.n_heads + it.h] =
                     empty ? -INFINITY : (m_ref + log2f(l_sum)) * 0.69314718055994531f;
+            // the O reads above complete before this thread's next P is published, and the
+            // next item's first P.V (which overwrites O) waits for that P
         }
     }
 
@@ -506,13 +594,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
 }
 
 template <int D>
-cudaError_t launch_d(const PrefillTcArgs &a, cudaStream_t s) {
+cudaError_t launch_d(const PrefillTcArgs &a, int num_sms, cudaStream_t s) {
     using C = TcCfg<D>;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    const int n_mtiles = (a.seq_len + kBM - 1) / kBM;
-    dim3 grid(a.n_heads * C::kSplitO, a.batch, n_mtiles);
+    const int64_t n_items = (int64_t)a.batch * a.n_heads * C::kSplitO * ((a.seq_len + kBM - 1) / kBM);
+    const int grid = (int)std::min<int64_t>(n_items, std::max(1, num_sms));  // one CTA per SM
     prefill_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(a);
     return cudaGetLastError();
 }
@@ -530,14 +618,14 @@ int prefill_tc_block_n(int head_dim) {
     }
 }
 
-cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s) {
+cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t s) {
     if (a.seq_len == 0 || a.batch == 0) return cudaSuccess;
     switch (a.head_dim) {
-        case 64: return launch_d<64>(a, s);
-        case 80: return launch_d<80>(a, s);
-        case 128: return launch_d<128>(a, s);
-        case 256: return launch_d<256>(a, s);
-        case 512: return launch_d<512>(a, s);
+        case 64: return launch_d<64>(a, num_sms, s);
+        case 80: return launch_d<80>(a, num_sms, s);
+        case 128: return launch_d<128>(a, num_sms, s);
+        case 256: return launch_d<256>(a, num_sms, s);
+        case 512: return launch_d<512>(a, num_sms, s);
         default: return cudaErrorInvalidValue;
     }
 }
