@@ -172,6 +172,18 @@ class Flusher:
         self.buf.zero_()
 
 
+def replica_throughput(ms_local, work, world, dist=None, device="cpu"):
+    """Whole-job throughput of `world` replicas that each processed `work` units in
+    `ms_local` milliseconds: the slowest rank (max over ranks) bounds the job, so the
+    value is world * work / max_ms.  Returns (max_ms, value)."""
+    ms = float(ms_local)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, work * world / (ms / 1e3)
+
+
 def time_steps(fn, steps, flush, stream):
     """Run `fn` `steps` times, L2 flushed before each; returns per-step ms (CUDA events
     recorded on the stream the kernels run on)."""
@@ -478,12 +490,6 @@ def main():
     if dist is not None:
         dist.barrier()
     step.check_status()
-    ms_total = sum(ms_steps)
-    if dist is not None:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
-    ms_per_step = ms_total / args.steps
     if wl.kind == "prefill":
         flops, alg_bytes, _ = prefill_work(wl)
         unit, work = "TFLOP/s", flops / 1e12
@@ -498,14 +504,11 @@ def main():
         kernel = "decode_bf16_kernel<%d>" % wl.D
         bound = "hbm"
         profile, srcs = "decode_bf16_%s.md" % wl.name, ["decode_bf16.cu", "device_common.cuh", "kernels.h"]
-    value = work * world / (ms_per_step / 1e3)
+    ms_total, _ = replica_throughput(sum(ms_steps), work, world, dist, device)
+    ms_per_step, value = replica_throughput(ms_total / args.steps, work, world)
 
     e2e_ms, h2d, d2h = e2e_measure(step, args.steps, stream)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = work * world / (e2e_ms / 1e3)
+    e2e_ms, e2e_value = replica_throughput(e2e_ms, work, world, dist, device)
 
     extra = None
     if not args.no_extra:
