@@ -53,16 +53,20 @@ constexpr int kKProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
 constexpr int kMmaWarp = 10;
 constexpr int kChunkCols = 64;       // head-dim columns per swizzled chunk (128 bytes)
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;       // O accumulator columns [0, 256)
-constexpr uint32_t kTmemS = 256;     // S buffers at 256 and 256 + BN
+constexpr uint32_t kTmemO = 0;       // O accumulator columns [0, kOCols)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct TcCfg {
     static constexpr int kQkChunks = (D + kChunkCols - 1) / kChunkCols;   // Q/K chunks
     static constexpr int kKSteps = (D + 15) / 16;                          // S MMA k-steps
-    static constexpr int kBN = D <= 256 ? 128 : 64;                        // keys per tile
+    // keys per tile; head_dim 64 takes 64-key tiles so that two CTAs fit one SM (256 tensor
+    // memory columns and under 113 KB of shared memory each): at that size a CTA's serial
+    // chain of S MMA, softmax and P.V leaves the SM idle, and a second CTA fills the gaps
+    static constexpr int kBN = D == 64 ? 64 : (D <= 256 ? 128 : 64);
+    static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
+    static constexpr uint32_t kTmemS = D == 64 ? 64 : 256;     // S buffers at kTmemS (+ BN)
+    static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
     static constexpr int kSplitO = D == 512 ? 2 : 1;                       // CTAs per O row
     static constexpr int kOCols = D / kSplitO;                             // O cols per CTA
     static constexpr int kVChunks = (kOCols + kChunkCols - 1) / kChunkCols;
@@ -82,7 +86,7 @@ struct TcCfg {
     static constexpr int kSlack = kPayload + 1024 <= 232448 ? 1024 : 0;
     static constexpr int kSmem = kSlack + kPayload;
     static_assert(kSmem <= 232448, "shared memory budget");
-    static_assert(kOCols <= 256 && kTmemS + 2 * kBN <= kTmemCols, "tensor memory budget");
+    static_assert(kOCols <= kTmemS && kTmemS + 2 * kBN <= kTmemCols, "tensor memory budget");
     static_assert(kBN % 32 == 0, "P columns per warpgroup must fill whole TMEM stores");
 };
 
@@ -177,7 +181,7 @@ __device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, TcCfg<D>::kCtasPerSm)
 prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     using C = TcCfg<D>;
     constexpr int BN = C::kBN;
@@ -236,7 +240,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         fence_mbarrier_init();
     }
     if (warp == kMmaWarp) {  // whole warp: allocate tensor memory
-        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -348,7 +352,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d_s = tmem + kTmemS + (uint32_t)((gt & 1) * BN);
+                        const uint32_t d_s = tmem + C::kTmemS + (uint32_t)((gt & 1) * BN);
                         const uint64_t dk = dk0 + (uint64_t)((s * C::kKTileBytes) >> 4);
 #pragma unroll
                         for (int c = 0; c < C::kQkChunks; ++c) {
@@ -379,7 +383,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                         }
                         tc_fence_after();
                         const uint64_t dv = sw128_desc_mn(smem_u32(sV) + s * C::kVTileBytes, C::kChunkBytes);
-                        const uint32_t p_tmem = tmem + kTmemS + (uint32_t)((gp & 1) * BN);
+                        const uint32_t p_tmem = tmem + C::kTmemS + (uint32_t)((gp & 1) * BN);
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
                             tc_mma_ts(tmem + kTmemO, p_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
@@ -450,7 +454,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                 float sv[HC];
 #pragma unroll
                 for (int c = 0; c < HC; c += 16)
-                    tmem_ld16(lane_base + kTmemS + (gt & 1) * BN + col0 + c,
+                    tmem_ld16(lane_base + C::kTmemS + (gt & 1) * BN + col0 + c,
                               reinterpret_cast<uint32_t *>(sv + c));
                 tc_wait_ld();
 
@@ -509,7 +513,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                 // warpgroups have read their S columns (the exchange above orders that),
                 // and P sits where its P.V MMA will read it
                 {
-                    const uint32_t pcol = lane_base + kTmemS + (gt & 1) * BN + col0 / 2;
+                    const uint32_t pcol = lane_base + C::kTmemS + (gt & 1) * BN + col0 / 2;
 #pragma unroll
                     for (int c = 0; c < HC / 2; c += 8) {
                         uint32_t pk[8];
@@ -589,7 +593,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     if (threadIdx.x == 0 && *abort_flag) report_status(a.status, kErrTimeout);
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
@@ -600,7 +604,7 @@ cudaError_t launch_d(const PrefillTcArgs &a, int num_sms, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t n_items = (int64_t)a.batch * a.n_heads * C::kSplitO * ((a.seq_len + kBM - 1) / kBM);
-    const int grid = (int)std::min<int64_t>(n_items, std::max(1, num_sms));  // one CTA per SM
+    const int grid = (int)std::min<int64_t>(n_items, std::max(1, num_sms) * C::kCtasPerSm);
     prefill_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(a);
     return cudaGetLastError();
 }
