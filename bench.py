@@ -43,6 +43,8 @@ import workloads as W  # noqa: E402
 METRIC = "GQA attention prefill TFLOP/s and decode KV GB/s, % of GB300 roofline"
 HEADLINE = "qwen3_0.6b_prefill"
 FLUSH_BYTES = 256 << 20
+L2_NOTE = ("flushed before every timed step: a 256 MiB write, then a 256 MiB read that "
+           "leaves no dirty lines to write back during the step")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -165,11 +167,19 @@ class ClockSampler:
 # ------------------------------------------------------------------------------ GPU arm
 
 class Flusher:
+    """Evicts the timed step's data from L2 before each step: a 256 MiB write (2x L2), then
+    a 256 MiB read of a second buffer, which pushes the written lines back to DRAM before
+    the step starts instead of during it (a write alone leaves ~L2-sized dirty data whose
+    write-back would compete with the step's own reads)."""
+
     def __init__(self, device):
         self.buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
 
     def __call__(self):
         self.buf.zero_()
+        torch.sum(self.rd, dim=0, out=self.sink)
 
 
 def replica_throughput(ms_local, work, world, dist=None, device="cpu"):
@@ -416,14 +426,14 @@ def workload_config(wl):
             "uniform[1,%d]" % wl.L if wl.kv_lens is None else str(wl.kv_lens), wl.dtype),
             "batch": wl.B, "kv_capacity": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
             "head_dim": wl.D, "window": wl.window,
-            "l2": "flushed before every timed step (256 MiB write)", "parallelism": "replicas"}
+            "l2": L2_NOTE, "parallelism": "replicas"}
     return {"workload": "%s: B%d S%d Hq%d Hkv%d D%d %s%s %s%s" % (
         wl.name, wl.B, wl.S, wl.Hq, wl.Hkv, wl.D, "causal" if wl.causal else "full",
         " window %d" % wl.window if wl.window else "", wl.dtype,
         ", packed QKV [%d, %d]" % (wl.B * wl.S, (wl.Hq + 2 * wl.Hkv) * wl.D) if wl.packed else ""),
         "batch": wl.B, "seq_len": wl.S, "kv_len": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
         "head_dim": wl.D, "causal": wl.causal, "window": wl.window,
-        "l2": "flushed before every timed step (256 MiB write)",
+        "l2": L2_NOTE,
         "parallelism": "replicas"}
 
 
