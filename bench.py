@@ -236,6 +236,41 @@ class PrefillStep:
             raise RuntimeError("device status %s" % self.b.lat_status_string(st))
 
 
+class PrefillCachedStep:
+    """A chunk of S new query rows per sequence against the first L rows of a token-major
+    KV cache of `cap` slots (slots past L hold NaN)."""
+
+    def __init__(self, wl, device):
+        from gqa_attention_lat_gb300 import binding
+        self.b = binding
+        self.wl = wl
+        self.di = W.decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.cap, kv_lens=wl.L,
+                                  dtype=wl.dtype, device=device, nan_fill=True)
+        self.q = W.normal((wl.B * wl.S, wl.Hq * wl.D), dtype=wl.dtype, device=device,
+                          seed=W.BASE_SEED, role="chunk_q")
+        self.out = torch.empty((wl.B * wl.S, wl.Hq * wl.D), dtype=W.torch_dtype(wl.dtype),
+                               device=device)
+        self.lse = torch.empty((wl.B * wl.S, wl.Hq), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.dt = binding.LAT_BF16 if wl.dtype == "bf16" else binding.LAT_F32
+
+    def __call__(self, q=None, k_cache=None, v_cache=None):
+        wl, d = self.wl, self.di
+        q = self.q if q is None else q
+        k_cache = d.k_cache if k_cache is None else k_cache
+        v_cache = d.v_cache if v_cache is None else v_cache
+        self.b.lat_attn_prefill_cached(self.dt, q, self.q.stride(0), k_cache, v_cache,
+                                       wl.Hkv * wl.D, wl.D, wl.cap * wl.Hkv * wl.D, self.out,
+                                       self.out.stride(0), self.lse, wl.B, wl.S, wl.L, wl.Hq,
+                                       wl.Hkv, wl.D, wl.causal, wl.window, wl.scale,
+                                       self.status)
+
+    def check_status(self):
+        st = int(self.status.item())
+        if st != 0:
+            raise RuntimeError("device status %s" % self.b.lat_status_string(st))
+
+
 class DecodeStep:
     def __init__(self, wl, device):
         from gqa_attention_lat_gb300 import binding
@@ -286,6 +321,22 @@ def measure_extra(device, flush, stream, peaks, reps=10):
                      "gflop": flops / 1e9}
         del step
         torch.cuda.empty_cache()
+    for name in ("qwen3_chunked_prefill",):
+        wl = W.WORKLOADS[name]
+        step = PrefillCachedStep(wl, device)
+        for _ in range(3):
+            step()
+        ms = time_steps(step, reps, flush, stream)
+        step.check_status()
+        flops, bytes_, _ = prefill_work(wl)
+        t = statistics.median(ms) / 1e3
+        tf = flops / t / 1e12
+        res[name] = {"kind": "prefill_cached", "ms": statistics.median(ms), "tflops": tf,
+                     "gbs": bytes_ / t / 1e9, "bound": "hbm",
+                     "frac_of_hbm_peak": bytes_ / t / 1e9 / peaks["hbm_gbs"],
+                     "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "gflop": flops / 1e9}
+        del step
+        torch.cuda.empty_cache()
     for name in ("decode_b32_h32_kv8_d128", "gemma4_global_decode"):
         wl = W.WORKLOADS[name]
         step = DecodeStep(wl, device)
@@ -313,6 +364,10 @@ def e2e_measure(step, steps, stream):
             parents = [inp.packed]
         else:
             parents = [inp.q.contiguous(), inp.k.contiguous(), inp.v.contiguous()]
+        outs = [step.out, step.lse]
+    elif isinstance(step, PrefillCachedStep):
+        d = step.di
+        parents = [step.q, d.k_cache, d.v_cache]
         outs = [step.out, step.lse]
     else:
         d = step.di
@@ -427,10 +482,15 @@ def workload_config(wl):
             "batch": wl.B, "kv_capacity": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
             "head_dim": wl.D, "window": wl.window,
             "l2": L2_NOTE, "parallelism": "replicas"}
+    where = ""
+    if wl.packed:
+        where = ", packed QKV [%d, %d]" % (wl.B * wl.S, (wl.Hq + 2 * wl.Hkv) * wl.D)
+    elif wl.kind == "prefill_cached":
+        where = ", K/V from a token-major cache [%d, %d, %d] (kv_len %d)" % (
+            wl.B, wl.cap, wl.Hkv * wl.D, wl.L)
     return {"workload": "%s: B%d S%d Hq%d Hkv%d D%d %s%s %s%s" % (
         wl.name, wl.B, wl.S, wl.Hq, wl.Hkv, wl.D, "causal" if wl.causal else "full",
-        " window %d" % wl.window if wl.window else "", wl.dtype,
-        ", packed QKV [%d, %d]" % (wl.B * wl.S, (wl.Hq + 2 * wl.Hkv) * wl.D) if wl.packed else ""),
+        " window %d" % wl.window if wl.window else "", wl.dtype, where),
         "batch": wl.B, "seq_len": wl.S, "kv_len": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
         "head_dim": wl.D, "causal": wl.causal, "window": wl.window,
         "l2": L2_NOTE,
@@ -483,7 +543,8 @@ def main():
     if wl.dtype != "bf16":
         raise SystemExit("bench workloads are bf16 (the fp32 shapes are parity cases)")
     flush = Flusher(device)
-    step = PrefillStep(wl, device) if wl.kind == "prefill" else DecodeStep(wl, device)
+    step = {"prefill": PrefillStep, "prefill_cached": PrefillCachedStep,
+            "decode": DecodeStep}[wl.kind](wl, device)
     sampler = ClockSampler(local)
     sampler.start()
     for _ in range(args.warmup):
@@ -500,7 +561,7 @@ def main():
     if dist is not None:
         dist.barrier()
     step.check_status()
-    if wl.kind == "prefill":
+    if wl.kind in ("prefill", "prefill_cached"):
         flops, alg_bytes, _ = prefill_work(wl)
         unit, work = "TFLOP/s", flops / 1e12
         kernel = "prefill_tc_kernel<%d>" % wl.D

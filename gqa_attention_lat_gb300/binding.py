@@ -38,6 +38,9 @@ _SIGNATURES = {
     "lat_status_string": (ctypes.c_char_p, [_I32]),
     "lat_attn_prefill": (_I32, [_I32, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P,
                                 _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P]),
+    "lat_attn_prefill_cached": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P,
+                                       _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P,
+                                       _P]),
     "lat_attn_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lat_attn_decode": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _I64,
                                _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _P]),
@@ -100,6 +103,17 @@ def lat_attn_prefill(dt, q, q_rs, k, k_rs, v, v_rs, out, out_rs, lse, batch, seq
         dt, _ptr(q), q_rs, _ptr(k), k_rs, _ptr(v), v_rs, _ptr(out), out_rs, _ptr(lse), batch,
         seq_len, kv_len, n_heads, n_kv_heads, head_dim, int(bool(causal)), window, scale,
         _ptr(status), _stream(stream)), "lat_attn_prefill")
+
+
+def lat_attn_prefill_cached(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                            cache_seq_stride, out, out_rs, lse, batch, seq_len, kv_len, n_heads,
+                            n_kv_heads, head_dim, causal, window, scale, status=None,
+                            stream=None):
+    _check(library().lat_attn_prefill_cached(
+        dt, _ptr(q), q_rs, _ptr(k_cache), _ptr(v_cache), cache_rs, cache_head_stride,
+        cache_seq_stride, _ptr(out), out_rs, _ptr(lse), batch, seq_len, kv_len, n_heads,
+        n_kv_heads, head_dim, int(bool(causal)), window, scale, _ptr(status), _stream(stream)),
+        "lat_attn_prefill_cached")
 
 
 def lat_attn_decode_workspace_size(dt, batch, n_heads, n_kv_heads, head_dim, max_kv_len) -> int:

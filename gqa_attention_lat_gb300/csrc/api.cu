@@ -59,7 +59,8 @@ bool make_head_map(CUtensorMap *m, const void *base, int head_dim, int heads, in
 // cache's own element strides, a [64, 1, box_rows, 1] box and 128-byte swizzle.
 bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int heads, int rows,
                     int batch, int64_t row_stride, int64_t head_stride, int64_t seq_stride,
-                    int box_rows) {
+                    int box_rows,
+                    CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows,
@@ -69,8 +70,7 @@ bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int heads, i
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -98,11 +98,16 @@ int current_sm_count(int *out) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s per CTA
 
-lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k, int64_t k_rs,
-                        const void *v, int64_t v_rs, void *out, int64_t out_rs, float *lse,
-                        int batch, int seq_len, int kv_len, int n_heads, int n_kv_heads,
-                        int head_dim, int causal, int window, float scale, int32_t *status,
-                        void *stream, uint64_t timeout_ns, int skip_kv_load) {
+// Where K and V element (b, j, hk, d) live: base + b*seq + j*row + hk*head + d (elements).
+struct KvStrides {
+    int64_t k_row, k_head, k_seq, v_row, v_head, v_seq;
+};
+
+lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k, const void *v,
+                        const KvStrides &kv, void *out, int64_t out_rs, float *lse, int batch,
+                        int seq_len, int kv_len, int n_heads, int n_kv_heads, int head_dim,
+                        int causal, int window, float scale, int32_t *status, void *stream,
+                        uint64_t timeout_ns, int skip_kv_load) {
     if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
     if (batch < 0 || seq_len < 0 || kv_len < seq_len || n_heads <= 0 || n_kv_heads <= 0 ||
         n_heads % n_kv_heads != 0)
@@ -112,7 +117,8 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
     if (batch == 0 || seq_len == 0) return LAT_OK;
     if (!q || !k || !v || !out) return LAT_ERR_INVALID_ARG;
     if (q_rs < (int64_t)n_heads * head_dim || out_rs < (int64_t)n_heads * head_dim ||
-        k_rs < (int64_t)n_kv_heads * head_dim || v_rs < (int64_t)n_kv_heads * head_dim)
+        kv.k_row <= 0 || kv.k_head <= 0 || kv.k_seq <= 0 || kv.v_row <= 0 || kv.v_head <= 0 ||
+        kv.v_seq <= 0)
         return LAT_ERR_INVALID_ARG;
     if (batch > 65535 || (seq_len + 127) / 128 > 65535) return LAT_ERR_UNSUPPORTED;
     if (window < 0) window = 0;
@@ -124,12 +130,12 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
         a.q_rs = q_rs;
         a.k = static_cast<const float *>(k);
         a.v = static_cast<const float *>(v);
-        a.k_seq = (int64_t)kv_len * k_rs;
-        a.k_row = k_rs;
-        a.k_head = head_dim;
-        a.v_seq = (int64_t)kv_len * v_rs;
-        a.v_row = v_rs;
-        a.v_head = head_dim;
+        a.k_seq = kv.k_seq;
+        a.k_row = kv.k_row;
+        a.k_head = kv.k_head;
+        a.v_seq = kv.v_seq;
+        a.v_row = kv.v_row;
+        a.v_head = kv.v_head;
         a.out = static_cast<float *>(out);
         a.out_rs = out_rs;
         a.lse = lse;
@@ -150,13 +156,18 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
 
     // bf16: tensor-memory-access reads need 16-byte aligned bases and row strides
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || q_rs % 8 ||
-        k_rs % 8 || v_rs % 8 || out_rs % 8)
+        out_rs % 8 || kv.k_row % 8 || kv.k_head % 8 || kv.k_seq % 8 || kv.v_row % 8 ||
+        kv.v_head % 8 || kv.v_seq % 8)
         return LAT_ERR_INVALID_ARG;
     lat::PrefillTcArgs a{};
     const int bn = lat::prefill_tc_block_n(head_dim);
+    // K/V maps span exactly kv_len rows per sequence: rows past it read as zeros, so cache
+    // slots beyond the visible keys (which may hold anything) never reach the MMA
     if (!make_head_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, 128) ||
-        !make_head_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, k_rs, bn) ||
-        !make_head_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, v_rs, bn))
+        !make_cache_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, kv.k_row, kv.k_head,
+                        kv.k_seq, bn, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
+        !make_cache_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, kv.v_row, kv.v_head,
+                        kv.v_seq, bn, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return LAT_ERR_CUDA;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.out_rs = out_rs;
@@ -200,7 +211,24 @@ lat_status lat_attn_prefill(lat_dtype dt, const void *q, int64_t q_rs, const voi
                             int64_t out_rs, float *lse, int batch, int seq_len, int kv_len,
                             int n_heads, int n_kv_heads, int head_dim, int causal, int window,
                             float scale, int32_t *status, void *stream) {
-    return prefill_impl(dt, q, q_rs, k, k_rs, v, v_rs, out, out_rs, lse, batch, seq_len,
+    if (k_rs < (int64_t)n_kv_heads * head_dim || v_rs < (int64_t)n_kv_heads * head_dim)
+        return LAT_ERR_INVALID_ARG;
+    const KvStrides kv{k_rs, head_dim, (int64_t)kv_len * k_rs, v_rs, head_dim, (int64_t)kv_len * v_rs};
+    return prefill_impl(dt, q, q_rs, k, v, kv, out, out_rs, lse, batch, seq_len, kv_len, n_heads,
+                        n_kv_heads, head_dim, causal, window, scale, status, stream,
+                        kDefaultTimeoutNs, 0);
+}
+
+lat_status lat_attn_prefill_cached(lat_dtype dt, const void *q, int64_t q_rs,
+                                   const void *k_cache, const void *v_cache, int64_t cache_rs,
+                                   int64_t cache_head_stride, int64_t cache_seq_stride,
+                                   void *out, int64_t out_rs, float *lse, int batch,
+                                   int seq_len, int kv_len, int n_heads, int n_kv_heads,
+                                   int head_dim, int causal, int window, float scale,
+                                   int32_t *status, void *stream) {
+    const KvStrides kv{cache_rs, cache_head_stride, cache_seq_stride,
+                       cache_rs, cache_head_stride, cache_seq_stride};
+    return prefill_impl(dt, q, q_rs, k_cache, v_cache, kv, out, out_rs, lse, batch, seq_len,
                         kv_len, n_heads, n_kv_heads, head_dim, causal, window, scale, status,
                         stream, kDefaultTimeoutNs, 0);
 }
@@ -210,9 +238,11 @@ lat_status lat_test_prefill_timeout(const void *q, int64_t q_rs, const void *k, 
                                     int batch, int seq_len, int n_heads, int n_kv_heads,
                                     int head_dim, uint64_t timeout_ns, int32_t *status,
                                     void *stream) {
-    return prefill_impl(LAT_BF16, q, q_rs, k, k_rs, v, v_rs, out, out_rs, nullptr, batch,
-                        seq_len, seq_len, n_heads, n_kv_heads, head_dim, 1, 0, 0.125f, status,
-                        stream, timeout_ns, 1);
+    const KvStrides kv{k_rs, head_dim, (int64_t)seq_len * k_rs, v_rs, head_dim,
+                       (int64_t)seq_len * v_rs};
+    return prefill_impl(LAT_BF16, q, q_rs, k, v, kv, out, out_rs, nullptr, batch, seq_len,
+                        seq_len, n_heads, n_kv_heads, head_dim, 1, 0, 0.125f, status, stream,
+                        timeout_ns, 1);
 }
 
 size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int n_kv_heads,

@@ -93,6 +93,31 @@ lat_status lat_attn_prefill(lat_dtype dt, const void *q, int64_t q_rs, const voi
                             int window, float scale, int32_t *status, void *stream);
 
 /*
+ * lat_attn_prefill_cached — lat_attn_prefill reading K and V from an in-place KV cache:
+ * a chunk of seq_len new query rows per sequence at positions kv_len - seq_len ..
+ * kv_len - 1, attending to cache rows 0 .. kv_len - 1 (the chunk's own keys appended
+ * first, e.g. by lat_kv_append).  This is the "full" (seq_len > 1) SDPA over a cache
+ * that the hf2q target page leaves open for chunked prefill (open question Q2), in the
+ * cache layout of its section 3.3.
+ *
+ * Layout: q, out and lse as in lat_attn_prefill; caches as in lat_attn_decode
+ *   (element (b,j,hk,d) at cache[b*cache_seq_stride + j*cache_rs + hk*cache_head_stride + d],
+ *   token-major or head-major).  Every sequence uses the same seq_len and kv_len
+ *   (kv_len >= seq_len) and its cache must hold at least kv_len rows; slots at or past
+ *   kv_len never reach the result (they may hold anything, NaN included).
+ * For LAT_BF16, q, out and the cache bases must be 16-byte aligned and q_rs, out_rs and
+ * the three cache strides multiples of 8, else LAT_ERR_INVALID_ARG.  Other rules and
+ * errors are those of lat_attn_prefill.
+ */
+lat_status lat_attn_prefill_cached(lat_dtype dt, const void *q, int64_t q_rs,
+                                   const void *k_cache, const void *v_cache, int64_t cache_rs,
+                                   int64_t cache_head_stride, int64_t cache_seq_stride,
+                                   void *out, int64_t out_rs, float *lse, int batch,
+                                   int seq_len, int kv_len, int n_heads, int n_kv_heads,
+                                   int head_dim, int causal, int window, float scale,
+                                   int32_t *status, void *stream);
+
+/*
  * lat_attn_decode_workspace_size — bytes of scratch lat_attn_decode needs for these
  * sizes (its split-KV partial results and merge counters).  Returns 0 for sizes the
  * library rejects.

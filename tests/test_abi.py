@@ -122,6 +122,36 @@ def test_workspace_size_rejects_bad_shapes(lib):
     assert binding.lat_attn_decode_workspace_size(LAT_BF16, 8, 16, 8, 96, 100) == 0
 
 
+def _prefill_cached(**kw):
+    args = dict(dt=LAT_BF16, q=FAKE, q_rs=1024, k_cache=FAKE, v_cache=FAKE, cache_rs=512,
+                cache_head_stride=128, cache_seq_stride=512 * 4096, out=FAKE, out_rs=1024,
+                lse=None, batch=2, seq_len=64, kv_len=300, n_heads=8, n_kv_heads=4,
+                head_dim=128, causal=1, window=0, scale=0.088)
+    args.update(kw)
+    return binding.lat_attn_prefill_cached(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kv_len=10), binding.LAT_ERR_INVALID_ARG),                    # kv_len < seq_len
+    (dict(n_heads=6), binding.LAT_ERR_INVALID_ARG),
+    (dict(head_dim=96, q_rs=768, out_rs=768), binding.LAT_ERR_UNSUPPORTED),
+    (dict(k_cache=None), binding.LAT_ERR_INVALID_ARG),
+    (dict(cache_seq_stride=0), binding.LAT_ERR_INVALID_ARG),
+    (dict(cache_head_stride=100), binding.LAT_ERR_INVALID_ARG),        # bf16 stride % 8
+    (dict(v_cache=FAKE + 8), binding.LAT_ERR_INVALID_ARG),            # bf16 misaligned
+    (dict(scale=float("inf")), binding.LAT_ERR_INVALID_ARG),
+])
+def test_prefill_cached_rejects_on_host(lib, kw, code):
+    with pytest.raises(binding.LatError) as e:
+        _prefill_cached(**kw)
+    assert e.value.status == code
+
+
+def test_prefill_cached_empty_is_a_no_op(lib):
+    _prefill_cached(seq_len=0)
+    _prefill_cached(batch=0)
+
+
 def _append(**kw):
     args = dict(dt=LAT_BF16, k_cache=FAKE, v_cache=FAKE, cache_rs=1024, cache_head_stride=128,
                 cache_seq_stride=1024 * 64, capacity=64, k_new=FAKE, v_new=FAKE, new_rs=1024,

@@ -24,7 +24,8 @@ import torch
 BASE_SEED = 0x1A7A77
 
 # independent generator streams per tensor role
-_STREAM = {"q": 1, "k": 2, "v": 3, "kv_len": 4, "cache": 5, "new": 6, "pos": 7, "rows": 8}
+_STREAM = {"q": 1, "k": 2, "v": 3, "kv_len": 4, "cache": 5, "new": 6, "pos": 7, "rows": 8,
+           "chunk_q": 9}
 
 
 def torch_dtype(name: str):
@@ -179,14 +180,15 @@ def sample_rows(n_rows_total: int, S: int, *, extra=(), n_random=256, seed=BASE_
 @dataclass
 class Workload:
     name: str
-    kind: str             # "prefill" or "decode"
+    kind: str             # "prefill", "prefill_cached" or "decode"
     dtype: str
     B: int
     Hq: int
     Hkv: int
     D: int
     S: int = 1            # prefill query length
-    L: int = 0            # prefill key length (= S) / decode cache capacity
+    L: int = 0            # prefill key length (>= S) / decode cache capacity
+    cap: int = 0          # prefill_cached: cache capacity (rows per sequence)
     causal: bool = True
     window: int = 0
     packed: bool = False
@@ -218,4 +220,8 @@ WORKLOADS = {
                                       512, S=8192, L=8192),
     "gemma4_global_decode": Workload("gemma4_global_decode", "decode", "bf16", 8, 16, 2, 512,
                                      L=32768, kv_lens=32768),
+    # chunked prefill against the decode cache: 512 new rows after 1536 cached keys, read
+    # from a token-major 4096-slot cache (Qwen3-0.6B attention shape)
+    "qwen3_chunked_prefill": Workload("qwen3_chunked_prefill", "prefill_cached", "bf16", 8, 16,
+                                      8, 64, S=512, L=2048, cap=4096),
 }
