@@ -7,9 +7,9 @@ numpy arrays into it.
 
 Functions
 ---------
-prefill(q, k, v, causal, window, scale, rows=None, threads=None)
+prefill(q, k, v, causal, window, scale, rows=None, threads=None, softcap=0.0)
     The attention definition for every query row (or a subset of rows).
-decode(q, k_cache, v_cache, kv_lens, window, scale)
+decode(q, k_cache, v_cache, kv_lens, window, scale, softcap=0.0)
     A decode step is the prefill definition with one query row whose position is the
     last cached key (query length 1, key length kv_len): the hf2q "Current Inference
     Path" page, section 3, runs the decode step as attention at seq_len 1 over the
@@ -70,12 +70,14 @@ class Oracle:
         fn.restype = ctypes.c_int
         P = ctypes.POINTER(ctypes.c_double)
         fn.argtypes = [P, P, P, P, P] + [ctypes.c_int] * 8 + [
-            ctypes.c_double, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int]
+            ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
+            ctypes.c_int]
         self._fn = fn
 
     def prefill(self, q, k, v, *, causal: bool, window: int, scale: float, rows=None,
-                threads=None):
-        """Softmax attention by definition, in double precision.
+                threads=None, softcap: float = 0.0):
+        """Softmax attention by definition, in double precision (scores capped as
+        softcap * tanh(s / softcap) when softcap > 0).
 
         q: [B, S, Hq, D]; k, v: [B, L, Hkv, D].  Returns (out, lse) with out
         [B, S, Hq, D] and lse [B, S, Hq] when ``rows`` is None, else out [n, Hq, D] and
@@ -98,7 +100,7 @@ class Oracle:
         rc = self._fn(
             q.ctypes.data_as(P), k.ctypes.data_as(P), v.ctypes.data_as(P),
             out.ctypes.data_as(P), lse.ctypes.data_as(P),
-            B, S, L, Hq, Hkv, D, int(bool(causal)), int(window), float(scale),
+            B, S, L, Hq, Hkv, D, int(bool(causal)), int(window), float(scale), float(softcap),
             rows_ptr, int(n_out) if rows is not None else 0,
             int(threads) if threads else default_threads())
         if rc != 0:
@@ -108,7 +110,7 @@ class Oracle:
         return out, lse
 
     def decode(self, q, k_cache, v_cache, kv_lens, *, window: int, scale: float,
-               threads=None):
+               threads=None, softcap: float = 0.0):
         """One decode step per sequence: q [B, Hq, D], caches [B, cap, Hkv, D].
 
         Sequence b attends to its first kv_lens[b] cached keys from query position
@@ -124,7 +126,8 @@ class Oracle:
             # only the visible prefix of each cache is converted (slots past n are unused)
             kb, vb = _f64(k_cache[b, :n]), _f64(v_cache[b, :n])
             o, l = self.prefill(q[b][None, None], kb[None], vb[None],
-                                causal=True, window=window, scale=scale, threads=threads)
+                                causal=True, window=window, scale=scale, threads=threads,
+                                softcap=softcap)
             out[b], lse[b] = o[0, 0], l[0, 0]
         return out, lse
 
@@ -137,14 +140,14 @@ def _get() -> Oracle:
     return _default
 
 
-def prefill(q, k, v, *, causal, window, scale, rows=None, threads=None):
+def prefill(q, k, v, *, causal, window, scale, rows=None, threads=None, softcap=0.0):
     return _get().prefill(q, k, v, causal=causal, window=window, scale=scale, rows=rows,
-                          threads=threads)
+                          threads=threads, softcap=softcap)
 
 
-def decode(q, k_cache, v_cache, kv_lens, *, window, scale, threads=None):
+def decode(q, k_cache, v_cache, kv_lens, *, window, scale, threads=None, softcap=0.0):
     return _get().decode(q, k_cache, v_cache, kv_lens, window=window, scale=scale,
-                         threads=threads)
+                         threads=threads, softcap=softcap)
 
 
 def kv_append(k_cache, v_cache, k_new, v_new, pos):

@@ -32,8 +32,12 @@
  *     - window W > 0: key j is visible iff p - j < W (W keys including self);
  *     - W <= 0 means no window.
  *
+ *   Softcap (larql page, section "BLAS-Fused Attention", step 2 "Scale + softcap", and
+ *   "Supported features": Gemma 2): when softcap > 0 the scaled score is replaced by
+ *   softcap * tanh(s / softcap) before the softmax; softcap <= 0 leaves it unchanged.
+ *
  *   Log-sum-exp (not on the pages; the build's reading): lse = m + ln(Z) with m the
- *   largest visible scaled score and Z = sum_j exp(s_j - m), natural logarithm.
+ *   largest visible (scaled, capped) score and Z = sum_j exp(s_j - m), natural logarithm.
  *   A row with no visible key has out = 0 and lse = -inf.
  *
  * Layouts (all row-major, contiguous, double):
@@ -58,7 +62,7 @@ typedef struct {
     double *out, *lse;
     int batch, seq_len, kv_len, n_heads, n_kv_heads, head_dim;
     int causal, window;
-    double scale;
+    double scale, softcap;
     const int64_t *rows;
     int64_t n_rows;
     int64_t unit_begin, unit_end; /* units are (output row t, head h) pairs */
@@ -96,6 +100,7 @@ static void attend_one(const oracle_job *jb, int64_t t, int h, double *scores) {
         double dot = 0.0;
         for (int d = 0; d < D; ++d) dot += qrow[d] * krow[d];
         scores[j] = jb->scale * dot;
+        if (jb->softcap > 0.0) scores[j] = jb->softcap * tanh(scores[j] / jb->softcap);
         if (scores[j] > m) m = scores[j];
         ++n_vis;
     }
@@ -136,7 +141,7 @@ static void *run_units(void *arg) {
 int oracle_attention_rows(const double *q, const double *k, const double *v, double *out,
                           double *lse, int batch, int seq_len, int kv_len, int n_heads,
                           int n_kv_heads, int head_dim, int causal, int window, double scale,
-                          const int64_t *rows, int64_t n_rows, int n_threads) {
+                          double softcap, const int64_t *rows, int64_t n_rows, int n_threads) {
     if (batch < 0 || seq_len < 0 || kv_len < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
         head_dim <= 0 || n_heads % n_kv_heads != 0)
         return -1;
@@ -164,7 +169,7 @@ int oracle_attention_rows(const double *q, const double *k, const double *v, dou
         jb->q = q; jb->k = k; jb->v = v; jb->out = out; jb->lse = lse;
         jb->batch = batch; jb->seq_len = seq_len; jb->kv_len = kv_len;
         jb->n_heads = n_heads; jb->n_kv_heads = n_kv_heads; jb->head_dim = head_dim;
-        jb->causal = causal; jb->window = window; jb->scale = scale;
+        jb->causal = causal; jb->window = window; jb->scale = scale; jb->softcap = softcap;
         jb->rows = rows; jb->n_rows = n_rows;
         jb->unit_begin = n_units * t / n_threads;
         jb->unit_end = n_units * (t + 1) / n_threads;

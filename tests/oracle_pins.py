@@ -8,7 +8,8 @@ AssertionError when the oracle disagrees with the mathematics:
   built visible-key matrix and the softmax taken in extended precision (long double),
   a separate code path from the oracle's row loop;
 - closed forms: one visible key returns that value row exactly; identical keys and a
-  zero scale return the mean of the visible values, lse = s + ln n;
+  zero scale return the mean of the visible values, lse = s + ln n; a softcap far above
+  every score changes nothing;
 - invariants: GQA equals multi-head attention with the KV heads repeated, a sliding
   window equals full attention with a materialised -inf mask, a decode step equals
   the last prefill row, adding a vector to every key shifts lse by scale*q.c and
@@ -59,8 +60,9 @@ def visible_matrix(S, L, causal, window):
     return vis
 
 
-def brute_force(q, k, v, causal, window, scale):
-    """Materialised softmax attention in long double.  q [B,S,Hq,D], k/v [B,L,Hkv,D]."""
+def brute_force(q, k, v, causal, window, scale, softcap=0.0):
+    """Materialised softmax attention in long double.  q [B,S,Hq,D], k/v [B,L,Hkv,D];
+    with softcap > 0 every scaled score s becomes softcap * tanh(s / softcap)."""
     B, S, Hq, D = q.shape
     L, Hkv = k.shape[1], k.shape[2]
     G = Hq // Hkv
@@ -74,6 +76,8 @@ def brute_force(q, k, v, causal, window, scale):
         for h in range(Hq):
             scores = ld(scale) * np.einsum("sd,ld->sl", q[b, :, h, :].astype(ld),
                                            k_rep[b, :, h, :])
+            if softcap > 0:
+                scores = ld(softcap) * np.tanh(scores / ld(softcap))
             scores = np.where(vis, scores, ld(-np.inf))
             for i in range(S):
                 if not vis[i].any():
@@ -108,7 +112,7 @@ def pin_golden(orc):
         k = np.array(c["k"], dtype=np.float64)[None]
         v = np.array(c["v"], dtype=np.float64)[None]
         out, lse = orc.prefill(q, k, v, causal=c["causal"], window=c["window"],
-                               scale=c["scale"])
+                               scale=c["scale"], softcap=c.get("softcap", 0.0))
         _close(out[0], np.array(c["out"]), 1e-12, c["name"] + " out")
         _close(lse[0], np.array(c["lse"]), 1e-12, c["name"] + " lse")
 
@@ -126,6 +130,9 @@ BRUTE_CASES = [
     (1, 5, 8, 5, 1, 4, True, 4),
 ]
 
+# (case, softcap): brute-force cases rerun with a score cap well inside the score range
+BRUTE_SOFTCAP = [(1, 0.5), (2, 1.3), (3, 0.8), (5, 2.0), (8, 0.3)]
+
 
 def pin_brute_force(orc):
     for n, (B, S, L, Hq, Hkv, D, causal, window) in enumerate(BRUTE_CASES):
@@ -138,6 +145,29 @@ def pin_brute_force(orc):
         bo, bl = brute_force(q, k, v, causal, window, scale)
         _close(out, bo, 1e-12, "brute force case %d out" % n)
         _close(lse, bl, 1e-12, "brute force case %d lse" % n)
+    for n, cap in BRUTE_SOFTCAP:
+        B, S, L, Hq, Hkv, D, causal, window = BRUTE_CASES[n]
+        r = _rng(300 + n)
+        q = 2.0 * r.standard_normal((B, S, Hq, D))  # scores of several units: the cap bites
+        k = r.standard_normal((B, L, Hkv, D))
+        v = r.standard_normal((B, L, Hkv, D))
+        out, lse = orc.prefill(q, k, v, causal=causal, window=window, scale=0.9, softcap=cap)
+        bo, bl = brute_force(q, k, v, causal, window, 0.9, softcap=cap)
+        _close(out, bo, 1e-12, "brute force softcap case %d out" % n)
+        _close(lse, bl, 1e-12, "brute force softcap case %d lse" % n)
+
+
+def pin_softcap_far_above_scores_is_no_cap(orc):
+    """tanh(x) = x - x^3/3 + ...: with every |s| <= 10 and a cap of 1e6 the capped score
+    differs from s by under 1e-9, so the result must match the uncapped one."""
+    r = _rng(11)
+    q = r.standard_normal((2, 6, 4, 8))
+    k = r.standard_normal((2, 6, 2, 8))
+    v = r.standard_normal((2, 6, 2, 8))
+    a_out, a_lse = orc.prefill(q, k, v, causal=True, window=0, scale=0.35)
+    b_out, b_lse = orc.prefill(q, k, v, causal=True, window=0, scale=0.35, softcap=1e6)
+    _close(b_out, a_out, 1e-8, "huge softcap out")
+    _close(b_lse, a_lse, 1e-8, "huge softcap lse")
 
 
 def pin_single_visible_key(orc):
@@ -288,4 +318,5 @@ def pin_key_permutation(orc):
 
 ALL_PINS = [pin_golden, pin_brute_force, pin_single_visible_key, pin_identical_keys,
             pin_zero_scale, pin_gqa_is_repeated_mha, pin_window_is_masked_softmax,
-            pin_decode_is_last_prefill_row, pin_key_shift, pin_key_permutation]
+            pin_decode_is_last_prefill_row, pin_key_shift, pin_key_permutation,
+            pin_softcap_far_above_scores_is_no_cap]

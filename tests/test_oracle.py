@@ -99,6 +99,12 @@ MUTATIONS = {
     "values_from_keys": ("const double *vrow = jb->v +", "const double *vrow = jb->k +"),
     "max_not_subtracted_in_lse": ("const double w = exp(scores[j] - m);",
                                   "const double w = exp(scores[j]);"),
+    "softcap_before_scale": (
+        "if (jb->softcap > 0.0) scores[j] = jb->softcap * tanh(scores[j] / jb->softcap);",
+        "if (jb->softcap > 0.0) scores[j] = jb->scale * jb->softcap * tanh(dot / jb->softcap);"),
+    "softcap_without_multiplier": (
+        "if (jb->softcap > 0.0) scores[j] = jb->softcap * tanh(scores[j] / jb->softcap);",
+        "if (jb->softcap > 0.0) scores[j] = tanh(scores[j] / jb->softcap);"),
     "wrong_batch_stride": ("(((int64_t)b * L + j) * jb->n_kv_heads + hk) * D;\n        double dot",
                            "(((int64_t)b * S + j) * jb->n_kv_heads + hk) * D;\n        double dot"),
 }
