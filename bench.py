@@ -226,6 +226,12 @@ class PrefillStep:
         q = i.q if q is None else q
         k = i.k if k is None else k
         v = i.v if v is None else v
+        if wl.softcap > 0:
+            self.b.lat_attn_prefill_softcap(self.dt, q, i.q.stride(0), k, i.k.stride(0), v,
+                                            i.v.stride(0), self.out, self.out.stride(0), self.lse,
+                                            wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, wl.causal,
+                                            wl.window, wl.scale, wl.softcap, self.status)
+            return
         self.b.lat_attn_prefill(self.dt, q, i.q.stride(0), k, i.k.stride(0), v, i.v.stride(0),
                                 self.out, self.out.stride(0), self.lse, wl.B, wl.S, wl.L, wl.Hq,
                                 wl.Hkv, wl.D, wl.causal, wl.window, wl.scale, self.status)
@@ -306,7 +312,7 @@ class DecodeStep:
 def measure_extra(device, flush, stream, peaks, reps=10):
     """The other named workloads, each against its own roofline."""
     res = {}
-    for name in ("gemma4_sliding_prefill", "gemma4_global_prefill"):
+    for name in ("gemma4_sliding_prefill", "gemma4_global_prefill", "gemma2_softcap_prefill"):
         wl = W.WORKLOADS[name]
         step = PrefillStep(wl, device)
         for _ in range(3):
@@ -490,7 +496,8 @@ def workload_config(wl):
             wl.B, wl.cap, wl.Hkv * wl.D, wl.L)
     return {"workload": "%s: B%d S%d Hq%d Hkv%d D%d %s%s %s%s" % (
         wl.name, wl.B, wl.S, wl.Hq, wl.Hkv, wl.D, "causal" if wl.causal else "full",
-        " window %d" % wl.window if wl.window else "", wl.dtype, where),
+        " window %d" % wl.window if wl.window else "", wl.dtype,
+        where + (", softcap %g" % wl.softcap if wl.softcap else "")),
         "batch": wl.B, "seq_len": wl.S, "kv_len": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
         "head_dim": wl.D, "causal": wl.causal, "window": wl.window,
         "l2": L2_NOTE,

@@ -41,6 +41,12 @@ _SIGNATURES = {
     "lat_attn_prefill_cached": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P,
                                        _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P,
                                        _P]),
+    "lat_attn_prefill_softcap": (_I32, [_I32, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P,
+                                        _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32,
+                                        _F32, _P, _P]),
+    "lat_attn_decode_softcap": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P,
+                                       _I64, _P, _I32, _I32, _I32, _I32, _I32, _F32, _F32, _P,
+                                       _SZ, _P, _P]),
     "lat_attn_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lat_attn_decode": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _I64,
                                _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _P]),
@@ -103,6 +109,26 @@ def lat_attn_prefill(dt, q, q_rs, k, k_rs, v, v_rs, out, out_rs, lse, batch, seq
         dt, _ptr(q), q_rs, _ptr(k), k_rs, _ptr(v), v_rs, _ptr(out), out_rs, _ptr(lse), batch,
         seq_len, kv_len, n_heads, n_kv_heads, head_dim, int(bool(causal)), window, scale,
         _ptr(status), _stream(stream)), "lat_attn_prefill")
+
+
+def lat_attn_prefill_softcap(dt, q, q_rs, k, k_rs, v, v_rs, out, out_rs, lse, batch, seq_len,
+                             kv_len, n_heads, n_kv_heads, head_dim, causal, window, scale,
+                             softcap, status=None, stream=None):
+    _check(library().lat_attn_prefill_softcap(
+        dt, _ptr(q), q_rs, _ptr(k), k_rs, _ptr(v), v_rs, _ptr(out), out_rs, _ptr(lse), batch,
+        seq_len, kv_len, n_heads, n_kv_heads, head_dim, int(bool(causal)), window, scale,
+        softcap, _ptr(status), _stream(stream)), "lat_attn_prefill_softcap")
+
+
+def lat_attn_decode_softcap(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                            cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch,
+                            n_heads, n_kv_heads, head_dim, window, scale, softcap, workspace,
+                            workspace_bytes, status=None, stream=None):
+    _check(library().lat_attn_decode_softcap(
+        dt, _ptr(q), q_rs, _ptr(k_cache), _ptr(v_cache), cache_rs, cache_head_stride,
+        cache_seq_stride, _ptr(kv_lens), max_kv_len, _ptr(out), out_rs, _ptr(lse), batch,
+        n_heads, n_kv_heads, head_dim, window, scale, softcap, _ptr(workspace),
+        workspace_bytes, _ptr(status), _stream(stream)), "lat_attn_decode_softcap")
 
 
 def lat_attn_prefill_cached(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,

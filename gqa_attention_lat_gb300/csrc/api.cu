@@ -106,9 +106,10 @@ struct KvStrides {
 lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k, const void *v,
                         const KvStrides &kv, void *out, int64_t out_rs, float *lse, int batch,
                         int seq_len, int kv_len, int n_heads, int n_kv_heads, int head_dim,
-                        int causal, int window, float scale, int32_t *status, void *stream,
-                        uint64_t timeout_ns, int skip_kv_load) {
+                        int causal, int window, float scale, float softcap, int32_t *status,
+                        void *stream, uint64_t timeout_ns, int skip_kv_load) {
     if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
+    if (!(softcap >= 0.f) || !isfinite(softcap)) return LAT_ERR_INVALID_ARG;
     if (batch < 0 || seq_len < 0 || kv_len < seq_len || n_heads <= 0 || n_kv_heads <= 0 ||
         n_heads % n_kv_heads != 0)
         return LAT_ERR_INVALID_ARG;
@@ -148,6 +149,7 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
         a.causal = causal != 0;
         a.window = window;
         a.scale = scale;
+        a.softcap = softcap;
         a.kv_lens = nullptr;
         a.max_kv_len = kv_len;
         a.status = status;
@@ -181,6 +183,8 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
     a.causal = causal != 0;
     a.window = window;
     a.scale_log2 = scale * kLog2e;
+    a.cap_log2 = softcap > 0.f ? softcap * kLog2e : 0.f;
+    a.raw_over_cap = softcap > 0.f ? scale / softcap : 0.f;
     a.status = status;
     a.timeout_ns = timeout_ns;
     a.test_skip_kv_load = skip_kv_load;
@@ -215,7 +219,21 @@ lat_status lat_attn_prefill(lat_dtype dt, const void *q, int64_t q_rs, const voi
         return LAT_ERR_INVALID_ARG;
     const KvStrides kv{k_rs, head_dim, (int64_t)kv_len * k_rs, v_rs, head_dim, (int64_t)kv_len * v_rs};
     return prefill_impl(dt, q, q_rs, k, v, kv, out, out_rs, lse, batch, seq_len, kv_len, n_heads,
-                        n_kv_heads, head_dim, causal, window, scale, status, stream,
+                        n_kv_heads, head_dim, causal, window, scale, 0.f, status, stream,
+                        kDefaultTimeoutNs, 0);
+}
+
+lat_status lat_attn_prefill_softcap(lat_dtype dt, const void *q, int64_t q_rs, const void *k,
+                                    int64_t k_rs, const void *v, int64_t v_rs, void *out,
+                                    int64_t out_rs, float *lse, int batch, int seq_len,
+                                    int kv_len, int n_heads, int n_kv_heads, int head_dim,
+                                    int causal, int window, float scale, float softcap,
+                                    int32_t *status, void *stream) {
+    if (k_rs < (int64_t)n_kv_heads * head_dim || v_rs < (int64_t)n_kv_heads * head_dim)
+        return LAT_ERR_INVALID_ARG;
+    const KvStrides kv{k_rs, head_dim, (int64_t)kv_len * k_rs, v_rs, head_dim, (int64_t)kv_len * v_rs};
+    return prefill_impl(dt, q, q_rs, k, v, kv, out, out_rs, lse, batch, seq_len, kv_len, n_heads,
+                        n_kv_heads, head_dim, causal, window, scale, softcap, status, stream,
                         kDefaultTimeoutNs, 0);
 }
 
@@ -229,7 +247,7 @@ lat_status lat_attn_prefill_cached(lat_dtype dt, const void *q, int64_t q_rs,
     const KvStrides kv{cache_rs, cache_head_stride, cache_seq_stride,
                        cache_rs, cache_head_stride, cache_seq_stride};
     return prefill_impl(dt, q, q_rs, k_cache, v_cache, kv, out, out_rs, lse, batch, seq_len,
-                        kv_len, n_heads, n_kv_heads, head_dim, causal, window, scale, status,
+                        kv_len, n_heads, n_kv_heads, head_dim, causal, window, scale, 0.f, status,
                         stream, kDefaultTimeoutNs, 0);
 }
 
@@ -241,7 +259,7 @@ lat_status lat_test_prefill_timeout(const void *q, int64_t q_rs, const void *k, 
     const KvStrides kv{k_rs, head_dim, (int64_t)seq_len * k_rs, v_rs, head_dim,
                        (int64_t)seq_len * v_rs};
     return prefill_impl(LAT_BF16, q, q_rs, k, v, kv, out, out_rs, nullptr, batch, seq_len,
-                        seq_len, n_heads, n_kv_heads, head_dim, 1, 0, 0.125f, status, stream,
+                        seq_len, n_heads, n_kv_heads, head_dim, 1, 0, 0.125f, 0.f, status, stream,
                         timeout_ns, 1);
 }
 
@@ -259,14 +277,19 @@ size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int 
     return plan.total_bytes;
 }
 
-lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
-                           const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,
-                           int64_t cache_seq_stride, const int32_t *kv_lens, int max_kv_len,
-                           void *out, int64_t out_rs, float *lse, int batch, int n_heads,
-                           int n_kv_heads, int head_dim, int window, float scale,
-                           void *workspace, size_t workspace_bytes, int32_t *status,
-                           void *stream) {
+}  // extern "C"
+
+namespace {
+
+lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
+                       const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,
+                       int64_t cache_seq_stride, const int32_t *kv_lens, int max_kv_len,
+                       void *out, int64_t out_rs, float *lse, int batch, int n_heads,
+                       int n_kv_heads, int head_dim, int window, float scale, float softcap,
+                       void *workspace, size_t workspace_bytes, int32_t *status,
+                       void *stream) {
     if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
+    if (!(softcap >= 0.f) || !isfinite(softcap)) return LAT_ERR_INVALID_ARG;
     if (batch < 0 || max_kv_len < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
         n_heads % n_kv_heads != 0)
         return LAT_ERR_INVALID_ARG;
@@ -302,6 +325,7 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
         a.causal = 1;
         a.window = window;
         a.scale = scale;
+        a.softcap = softcap;
         a.kv_lens = kv_lens;
         a.max_kv_len = max_kv_len;
         a.status = status;
@@ -349,6 +373,8 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
     a.head_dim = head_dim;
     a.window = window;
     a.scale_log2 = scale * kLog2e;
+    a.cap_log2 = softcap > 0.f ? softcap * kLog2e : 0.f;
+    a.raw_over_cap = softcap > 0.f ? scale / softcap : 0.f;
     a.part_o = reinterpret_cast<float *>(ws);
     a.part_lse = reinterpret_cast<float *>(ws + plan.part_o_bytes);
     a.counters = reinterpret_cast<int32_t *>(ws + plan.part_o_bytes + plan.part_lse_bytes);
@@ -356,6 +382,37 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
     a.min_seg = plan.min_seg;
     a.status = status;
     return lat::launch_decode_bf16(a, plan.grid, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
+                           const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,
+                           int64_t cache_seq_stride, const int32_t *kv_lens, int max_kv_len,
+                           void *out, int64_t out_rs, float *lse, int batch, int n_heads,
+                           int n_kv_heads, int head_dim, int window, float scale,
+                           void *workspace, size_t workspace_bytes, int32_t *status,
+                           void *stream) {
+    return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                       cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
+                       n_kv_heads, head_dim, window, scale, 0.f, workspace, workspace_bytes,
+                       status, stream);
+}
+
+lat_status lat_attn_decode_softcap(lat_dtype dt, const void *q, int64_t q_rs,
+                                   const void *k_cache, const void *v_cache, int64_t cache_rs,
+                                   int64_t cache_head_stride, int64_t cache_seq_stride,
+                                   const int32_t *kv_lens, int max_kv_len, void *out,
+                                   int64_t out_rs, float *lse, int batch, int n_heads,
+                                   int n_kv_heads, int head_dim, int window, float scale,
+                                   float softcap, void *workspace, size_t workspace_bytes,
+                                   int32_t *status, void *stream) {
+    return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                       cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
+                       n_kv_heads, head_dim, window, scale, softcap, workspace, workspace_bytes,
+                       status, stream);
 }
 
 lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,

@@ -390,13 +390,20 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                     }
                 }
             }
-            // scale into the log2 domain and mask keys past the piece
+            // scale (and cap) into the log2 domain and mask keys past the piece
+            if (a.cap_log2 > 0.f) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[e] = a.cap_log2 * tanhf(sc[e] * a.raw_over_cap);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[e] *= a.scale_log2;
+            }
             const int key_a = r.key0 + row0 + (lane >> 2);
             const bool va = key_a < r.ke, vb = key_a + 8 < r.ke;
-            sc[0] = va ? sc[0] * a.scale_log2 : -INFINITY;
-            sc[1] = va ? sc[1] * a.scale_log2 : -INFINITY;
-            sc[2] = vb ? sc[2] * a.scale_log2 : -INFINITY;
-            sc[3] = vb ? sc[3] * a.scale_log2 : -INFINITY;
+            sc[0] = va ? sc[0] : -INFINITY;
+            sc[1] = va ? sc[1] : -INFINITY;
+            sc[2] = vb ? sc[2] : -INFINITY;
+            sc[3] = vb ? sc[3] : -INFINITY;
 
             float p[4], corr[2];
             bool refresh_any = false;

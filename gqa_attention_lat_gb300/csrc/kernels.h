@@ -35,6 +35,7 @@ struct RowAttnArgs {
     float *lse;
     int batch, seq_len, kv_len, n_heads, n_kv_heads, head_dim, causal, window;
     float scale;
+    float softcap;                 // > 0: score s becomes softcap * tanh(s / softcap)
     const int32_t *kv_lens;
     int max_kv_len;
     int32_t *status;
@@ -56,6 +57,7 @@ struct DecodeArgs {
     float *lse;
     int batch, n_heads, n_kv_heads, head_dim, window;
     float scale_log2;   // scale * log2(e): scores are exponentiated with exp2
+    float cap_log2, raw_over_cap;  // score cap, as in PrefillTcArgs (cap_log2 0: none)
     // split-KV scratch: partial outputs, partial lse and arrival counters
     float *part_o;      // [batch, n_heads, max_splits, head_dim]
     float *part_lse;    // [batch, n_heads, max_splits]
@@ -82,6 +84,9 @@ struct PrefillTcArgs {
     float *lse;
     int batch, seq_len, kv_len, n_heads, n_kv_heads, head_dim, causal, window;
     float scale_log2;              // scale * log2(e)
+    // score cap: when cap_log2 > 0 a raw dot product x scores cap_log2 * tanh(x * raw_over_cap)
+    // in the log2 domain (softcap * log2(e) and scale / softcap), replacing x * scale_log2
+    float cap_log2, raw_over_cap;
     int32_t *status;
     uint64_t timeout_ns;
     int test_skip_kv_load;         // test hook: never load KV tile 0 (forces a timeout)

@@ -415,7 +415,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         const int row = quarter * 32 + lane;          // query row in the tile = TMEM lane
         const int col0 = wg * HC;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sl2 = a.scale_log2;
+        const bool capped = a.cap_log2 > 0.f;
+        const float sl2 = capped ? 1.f : a.scale_log2;  // capped scores arrive pre-scaled
         const bool max_mode = sl2 >= 0.f;             // a negative scale flips max and min
         const float hide = max_mode ? -INFINITY : INFINITY;  // raw value that never wins
         bool ok = true;
@@ -457,6 +458,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     tmem_ld16(lane_base + C::kTmemS + (gt & 1) * BN + col0 + c,
                               reinterpret_cast<uint32_t *>(sv + c));
                 tc_wait_ld();
+                if (capped) {  // Gemma 2 score cap, in the log2 domain
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) sv[c] = a.cap_log2 * tanhf(sv[c] * a.raw_over_cap);
+                }
 
                 const int key0 = (it.band.t_begin + t) * BN;
                 const bool need_mask = (key0 + BN > a.kv_len) || (a.causal && key0 + BN - 1 > p_min) ||

@@ -3,7 +3,9 @@
 //
 // The arithmetic is the row-wise online softmax of the lattice-inference DESIGN page
 // ("Current Design": fused attention, online softmax in registers): keys are visited in
-// order, each score s = scale * q.k is reduced across the warp, and the running maximum
+// order, each score s = scale * q.k is reduced across the warp (then capped as
+// softcap * tanh(s / softcap) when a cap is set: the larql page, "BLAS-Fused Attention",
+// step 2), and the running maximum
 // m, normaliser l and output accumulator o are updated as
 //   m' = max(m, s),  l' = l*e^(m-m') + e^(s-m'),  o' = o*e^(m-m') + e^(s-m')*v.
 // fp32 inputs keep fp32 products (no tf32), so the result stays within ~1e-6 of fp64.
@@ -60,7 +62,8 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        const float s = part * a.scale;
+        float s = part * a.scale;
+        if (a.softcap > 0.f) s = a.softcap * tanhf(s / a.softcap);  // Gemma 2 score cap
         const float m_new = fmaxf(m, s);
         const float corr = expf(m - m_new);
         const float w = expf(s - m_new);

@@ -93,6 +93,21 @@ lat_status lat_attn_prefill(lat_dtype dt, const void *q, int64_t q_rs, const voi
                             int window, float scale, int32_t *status, void *stream);
 
 /*
+ * lat_attn_prefill_softcap — lat_attn_prefill with the Gemma 2 score cap: each scaled
+ * score s is replaced by softcap * tanh(s / softcap) before the softmax (the larql
+ * "Inference Engine" page, section "BLAS-Fused Attention", step 2, "Scale + softcap",
+ * listed there as a supported Gemma 2 feature).  softcap must be finite and >= 0; 0 means
+ * no cap (the result of lat_attn_prefill); otherwise LAT_ERR_INVALID_ARG.  The lse is
+ * taken over the capped scores.  All other arguments and rules are lat_attn_prefill's.
+ */
+lat_status lat_attn_prefill_softcap(lat_dtype dt, const void *q, int64_t q_rs, const void *k,
+                                    int64_t k_rs, const void *v, int64_t v_rs, void *out,
+                                    int64_t out_rs, float *lse, int batch, int seq_len,
+                                    int kv_len, int n_heads, int n_kv_heads, int head_dim,
+                                    int causal, int window, float scale, float softcap,
+                                    int32_t *status, void *stream);
+
+/*
  * lat_attn_prefill_cached — lat_attn_prefill reading K and V from an in-place KV cache:
  * a chunk of seq_len new query rows per sequence at positions kv_len - seq_len ..
  * kv_len - 1, attending to cache rows 0 .. kv_len - 1 (the chunk's own keys appended
@@ -168,6 +183,19 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
                            int n_kv_heads, int head_dim, int window, float scale,
                            void *workspace, size_t workspace_bytes, int32_t *status,
                            void *stream);
+
+/*
+ * lat_attn_decode_softcap — lat_attn_decode with the score cap of lat_attn_prefill_softcap
+ * (softcap finite and >= 0, 0 = none).  Same arguments, workspace and rules otherwise.
+ */
+lat_status lat_attn_decode_softcap(lat_dtype dt, const void *q, int64_t q_rs,
+                                   const void *k_cache, const void *v_cache, int64_t cache_rs,
+                                   int64_t cache_head_stride, int64_t cache_seq_stride,
+                                   const int32_t *kv_lens, int max_kv_len, void *out,
+                                   int64_t out_rs, float *lse, int batch, int n_heads,
+                                   int n_kv_heads, int head_dim, int window, float scale,
+                                   float softcap, void *workspace, size_t workspace_bytes,
+                                   int32_t *status, void *stream);
 
 /*
  * lat_attn_decode_static — lat_attn_decode without a caller workspace.  The pages have

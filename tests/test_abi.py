@@ -122,6 +122,19 @@ def test_workspace_size_rejects_bad_shapes(lib):
     assert binding.lat_attn_decode_workspace_size(LAT_BF16, 8, 16, 8, 96, 100) == 0
 
 
+@pytest.mark.parametrize("cap", [-1.0, float("inf"), float("nan")])
+def test_softcap_must_be_finite_and_non_negative(lib, cap):
+    with pytest.raises(binding.LatError) as e:
+        binding.lat_attn_prefill_softcap(LAT_BF16, FAKE, 1024, FAKE, 512, FAKE, 512, FAKE, 1024,
+                                         None, 1, 4, 4, 16, 8, 64, 1, 0, 0.125, cap)
+    assert e.value.status == binding.LAT_ERR_INVALID_ARG
+    with pytest.raises(binding.LatError) as e:
+        binding.lat_attn_decode_softcap(LAT_BF16, FAKE, 4096, FAKE, FAKE, 1024, 128,
+                                        4096 * 1024, FAKE, 4096, FAKE, 4096, None, 32, 32, 8,
+                                        128, 0, 0.088, cap, FAKE, 1 << 30)
+    assert e.value.status == binding.LAT_ERR_INVALID_ARG
+
+
 def _prefill_cached(**kw):
     args = dict(dt=LAT_BF16, q=FAKE, q_rs=1024, k_cache=FAKE, v_cache=FAKE, cache_rs=512,
                 cache_head_stride=128, cache_seq_stride=512 * 4096, out=FAKE, out_rs=1024,

@@ -189,6 +189,7 @@ class Workload:
     S: int = 1            # prefill query length
     L: int = 0            # prefill key length (>= S) / decode cache capacity
     cap: int = 0          # prefill_cached: cache capacity (rows per sequence)
+    softcap: float = 0.0  # > 0: Gemma 2 score cap softcap * tanh(s / softcap)
     causal: bool = True
     window: int = 0
     packed: bool = False
@@ -220,6 +221,9 @@ WORKLOADS = {
                                       512, S=8192, L=8192),
     "gemma4_global_decode": Workload("gemma4_global_decode", "decode", "bf16", 8, 16, 2, 512,
                                      L=32768, kv_lens=32768),
+    # Gemma-2-shaped global layer with its attention score cap of 50
+    "gemma2_softcap_prefill": Workload("gemma2_softcap_prefill", "prefill", "bf16", 1, 16, 8,
+                                       256, S=8192, L=8192, softcap=50.0),
     # chunked prefill against the decode cache: 512 new rows after 1536 cached keys, read
     # from a token-major 4096-slot cache (Qwen3-0.6B attention shape)
     "qwen3_chunked_prefill": Workload("qwen3_chunked_prefill", "prefill_cached", "bf16", 8, 16,
