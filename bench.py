@@ -282,8 +282,12 @@ class DecodeStep:
         from gqa_attention_lat_gb300 import binding
         self.b = binding
         self.wl = wl
-        self.di = W.decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.L, kv_lens=wl.kv_lens,
-                                  dtype=wl.dtype, device=device, nan_fill=True)
+        if wl.ring:
+            self.di = W.ring_decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.ring, wl.max_len,
+                                           dtype=wl.dtype, device=device)
+        else:
+            self.di = W.decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.L, kv_lens=wl.kv_lens,
+                                      dtype=wl.dtype, device=device, nan_fill=True)
         self.dt = binding.LAT_BF16 if wl.dtype == "bf16" else binding.LAT_F32
         self.nbytes = binding.lat_attn_decode_workspace_size(self.dt, wl.B, wl.Hq, wl.Hkv, wl.D,
                                                              wl.L)
@@ -298,6 +302,13 @@ class DecodeStep:
         k_cache = d.k_cache if k_cache is None else k_cache
         v_cache = d.v_cache if v_cache is None else v_cache
         kv_lens = d.kv_lens if kv_lens is None else kv_lens
+        if wl.ring:
+            self.b.lat_attn_decode_ring(self.dt, q, d.q.stride(0), k_cache, v_cache,
+                                        wl.Hkv * wl.D, wl.D, wl.L * wl.Hkv * wl.D, wl.ring,
+                                        kv_lens, wl.max_len, self.out, self.out.stride(0),
+                                        self.lse, wl.B, wl.Hq, wl.Hkv, wl.D, wl.window,
+                                        wl.scale, self.ws, self.nbytes, self.status)
+            return
         self.b.lat_attn_decode(self.dt, q, d.q.stride(0), k_cache, v_cache, wl.Hkv * wl.D,
                                wl.D, wl.L * wl.Hkv * wl.D, kv_lens, wl.L, self.out,
                                self.out.stride(0), self.lse, wl.B, wl.Hq, wl.Hkv, wl.D,
@@ -343,7 +354,7 @@ def measure_extra(device, flush, stream, peaks, reps=10):
                      "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "gflop": flops / 1e9}
         del step
         torch.cuda.empty_cache()
-    for name in ("decode_b32_h32_kv8_d128", "gemma4_global_decode"):
+    for name in ("decode_b32_h32_kv8_d128", "gemma4_global_decode", "gemma4_sliding_decode_ring"):
         wl = W.WORKLOADS[name]
         step = DecodeStep(wl, device)
         for _ in range(3):
@@ -482,9 +493,11 @@ def run_reference(args, rank, world):
 
 def workload_config(wl):
     if wl.kind == "decode":
-        return {"workload": "%s: decode B%d Hq%d Hkv%d D%d cache %d, kv_len %s %s" % (
-            wl.name, wl.B, wl.Hq, wl.Hkv, wl.D, wl.L,
-            "uniform[1,%d]" % wl.L if wl.kv_lens is None else str(wl.kv_lens), wl.dtype),
+        lens = "uniform[1,%d]" % (wl.max_len if wl.ring else wl.L) if wl.kv_lens is None \
+            else str(wl.kv_lens)
+        return {"workload": "%s: decode B%d Hq%d Hkv%d D%d %s %d, kv_len %s%s %s" % (
+            wl.name, wl.B, wl.Hq, wl.Hkv, wl.D, "ring cache" if wl.ring else "cache", wl.L,
+            lens, " window %d" % wl.window if wl.window else "", wl.dtype),
             "batch": wl.B, "kv_capacity": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
             "head_dim": wl.D, "window": wl.window,
             "l2": L2_NOTE, "parallelism": "replicas"}

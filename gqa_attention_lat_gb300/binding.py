@@ -47,6 +47,11 @@ _SIGNATURES = {
     "lat_attn_decode_softcap": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P,
                                        _I64, _P, _I32, _I32, _I32, _I32, _I32, _F32, _F32, _P,
                                        _SZ, _P, _P]),
+    "lat_attn_decode_ring": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _I32, _P, _I32,
+                                    _P, _I64, _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ,
+                                    _P, _P]),
+    "lat_kv_append_ring": (_I32, [_I32, _P, _P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _I32,
+                                  _I32, _I32, _I32, _P, _P]),
     "lat_attn_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lat_attn_decode": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _I64,
                                _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _P]),
@@ -129,6 +134,26 @@ def lat_attn_decode_softcap(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_
         cache_seq_stride, _ptr(kv_lens), max_kv_len, _ptr(out), out_rs, _ptr(lse), batch,
         n_heads, n_kv_heads, head_dim, window, scale, softcap, _ptr(workspace),
         workspace_bytes, _ptr(status), _stream(stream)), "lat_attn_decode_softcap")
+
+
+def lat_attn_decode_ring(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                         cache_seq_stride, ring_capacity, kv_lens, max_kv_len, out, out_rs, lse,
+                         batch, n_heads, n_kv_heads, head_dim, window, scale, workspace,
+                         workspace_bytes, status=None, stream=None):
+    _check(library().lat_attn_decode_ring(
+        dt, _ptr(q), q_rs, _ptr(k_cache), _ptr(v_cache), cache_rs, cache_head_stride,
+        cache_seq_stride, ring_capacity, _ptr(kv_lens), max_kv_len, _ptr(out), out_rs,
+        _ptr(lse), batch, n_heads, n_kv_heads, head_dim, window, scale, _ptr(workspace),
+        workspace_bytes, _ptr(status), _stream(stream)), "lat_attn_decode_ring")
+
+
+def lat_kv_append_ring(dt, k_cache, v_cache, cache_rs, cache_head_stride, cache_seq_stride,
+                       ring_capacity, k_new, v_new, new_rs, pos, n_new, batch, n_kv_heads,
+                       head_dim, status=None, stream=None):
+    _check(library().lat_kv_append_ring(
+        dt, _ptr(k_cache), _ptr(v_cache), cache_rs, cache_head_stride, cache_seq_stride,
+        ring_capacity, _ptr(k_new), _ptr(v_new), new_rs, _ptr(pos), n_new, batch, n_kv_heads,
+        head_dim, _ptr(status), _stream(stream)), "lat_kv_append_ring")
 
 
 def lat_attn_prefill_cached(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,

@@ -286,10 +286,12 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
                        int64_t cache_seq_stride, const int32_t *kv_lens, int max_kv_len,
                        void *out, int64_t out_rs, float *lse, int batch, int n_heads,
                        int n_kv_heads, int head_dim, int window, float scale, float softcap,
-                       void *workspace, size_t workspace_bytes, int32_t *status,
+                       int ring, void *workspace, size_t workspace_bytes, int32_t *status,
                        void *stream) {
     if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
     if (!(softcap >= 0.f) || !isfinite(softcap)) return LAT_ERR_INVALID_ARG;
+    // a ring cache keeps only the last `ring` positions: the window must fit in it
+    if (ring < 0 || (ring > 0 && (window <= 0 || window > ring))) return LAT_ERR_INVALID_ARG;
     if (batch < 0 || max_kv_len < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
         n_heads % n_kv_heads != 0)
         return LAT_ERR_INVALID_ARG;
@@ -328,6 +330,7 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
         a.softcap = softcap;
         a.kv_lens = kv_lens;
         a.max_kv_len = max_kv_len;
+        a.ring = ring;
         a.status = status;
         return lat::launch_row_attention_f32(a, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
     }
@@ -337,9 +340,11 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
         return LAT_ERR_INVALID_ARG;
     int sms = 0;
     if (!current_sm_count(&sms)) return LAT_ERR_CUDA;
+    // rows per sequence: the ring, or every position up to max_kv_len; the scratch layout
+    // is sized by the same count (a ring's visible keys never exceed it)
+    const int rows = ring > 0 ? ring : max_kv_len;
     lat::DecodePlan plan;
-    if (!lat::plan_decode_bf16(batch, n_heads, n_kv_heads, head_dim, max_kv_len, window, sms,
-                               &plan))
+    if (!lat::plan_decode_bf16(batch, n_heads, n_kv_heads, head_dim, rows, window, sms, &plan))
         return LAT_ERR_UNSUPPORTED;
     if (workspace == nullptr || workspace_bytes < plan.total_bytes ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -348,9 +353,9 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
     lat::DecodeArgs a{};
     if (max_kv_len > 0) {
         const int box = lat::decode_bf16_tile_keys(head_dim);
-        if (!make_cache_map(&a.tm_k, k_cache, head_dim, n_kv_heads, max_kv_len, batch, cache_rs,
+        if (!make_cache_map(&a.tm_k, k_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
                             cache_head_stride, cache_seq_stride, box) ||
-            !make_cache_map(&a.tm_v, v_cache, head_dim, n_kv_heads, max_kv_len, batch, cache_rs,
+            !make_cache_map(&a.tm_v, v_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
                             cache_head_stride, cache_seq_stride, box) ||
             !make_query_map(&a.tm_q, q, head_dim, n_heads, batch, q_rs))
             return LAT_ERR_CUDA;
@@ -372,6 +377,7 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
     a.n_kv_heads = n_kv_heads;
     a.head_dim = head_dim;
     a.window = window;
+    a.ring = ring;
     a.scale_log2 = scale * kLog2e;
     a.cap_log2 = softcap > 0.f ? softcap * kLog2e : 0.f;
     a.raw_over_cap = softcap > 0.f ? scale / softcap : 0.f;
@@ -397,8 +403,23 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
                            void *stream) {
     return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
                        cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
-                       n_kv_heads, head_dim, window, scale, 0.f, workspace, workspace_bytes,
-                       status, stream);
+                       n_kv_heads, head_dim, window, scale, 0.f, 0, workspace,
+                       workspace_bytes, status, stream);
+}
+
+lat_status lat_attn_decode_ring(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
+                                const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,
+                                int64_t cache_seq_stride, int ring_capacity,
+                                const int32_t *kv_lens, int max_kv_len, void *out,
+                                int64_t out_rs, float *lse, int batch, int n_heads,
+                                int n_kv_heads, int head_dim, int window, float scale,
+                                void *workspace, size_t workspace_bytes, int32_t *status,
+                                void *stream) {
+    if (ring_capacity <= 0) return LAT_ERR_INVALID_ARG;
+    return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                       cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
+                       n_kv_heads, head_dim, window, scale, 0.f, ring_capacity, workspace,
+                       workspace_bytes, status, stream);
 }
 
 lat_status lat_attn_decode_softcap(lat_dtype dt, const void *q, int64_t q_rs,
@@ -411,17 +432,22 @@ lat_status lat_attn_decode_softcap(lat_dtype dt, const void *q, int64_t q_rs,
                                    int32_t *status, void *stream) {
     return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
                        cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
-                       n_kv_heads, head_dim, window, scale, softcap, workspace, workspace_bytes,
-                       status, stream);
+                       n_kv_heads, head_dim, window, scale, softcap, 0, workspace,
+                       workspace_bytes, status, stream);
 }
 
-lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
-                         int64_t cache_head_stride, int64_t cache_seq_stride, int capacity,
-                         const void *k_new, const void *v_new, int64_t new_rs,
-                         const int32_t *pos, int n_new, int batch, int n_kv_heads,
-                         int head_dim, int32_t *status, void *stream) {
+}  // extern "C"
+
+namespace {
+
+lat_status append_impl(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
+                       int64_t cache_head_stride, int64_t cache_seq_stride, int capacity,
+                       const void *k_new, const void *v_new, int64_t new_rs, const int32_t *pos,
+                       int n_new, int batch, int n_kv_heads, int head_dim, int ring,
+                       int32_t *status, void *stream) {
     if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
     if (batch < 0 || n_new < 0 || capacity < 0 || n_kv_heads <= 0) return LAT_ERR_INVALID_ARG;
+    if (ring > 0 && n_new > ring) return LAT_ERR_INVALID_ARG;  // rows would overwrite each other
     if (!supported_head_dim(head_dim)) return LAT_ERR_UNSUPPORTED;
     if (batch == 0 || n_new == 0) return LAT_OK;
     if (!k_cache || !v_cache || !k_new || !v_new || !pos) return LAT_ERR_INVALID_ARG;
@@ -444,10 +470,36 @@ lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cac
     a.n_kv_heads = n_kv_heads;
     a.head_dim = head_dim;
     a.elem_bytes = dt == LAT_F32 ? 4 : 2;
+    a.ring = ring;
     a.status = status;
     return lat::launch_kv_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? LAT_OK
                : LAT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
+                         int64_t cache_head_stride, int64_t cache_seq_stride, int capacity,
+                         const void *k_new, const void *v_new, int64_t new_rs,
+                         const int32_t *pos, int n_new, int batch, int n_kv_heads,
+                         int head_dim, int32_t *status, void *stream) {
+    return append_impl(dt, k_cache, v_cache, cache_rs, cache_head_stride, cache_seq_stride,
+                       capacity, k_new, v_new, new_rs, pos, n_new, batch, n_kv_heads, head_dim,
+                       0, status, stream);
+}
+
+lat_status lat_kv_append_ring(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
+                              int64_t cache_head_stride, int64_t cache_seq_stride,
+                              int ring_capacity, const void *k_new, const void *v_new,
+                              int64_t new_rs, const int32_t *pos, int n_new, int batch,
+                              int n_kv_heads, int head_dim, int32_t *status, void *stream) {
+    if (ring_capacity <= 0) return LAT_ERR_INVALID_ARG;
+    return append_impl(dt, k_cache, v_cache, cache_rs, cache_head_stride, cache_seq_stride,
+                       ring_capacity, k_new, v_new, new_rs, pos, n_new, batch, n_kv_heads,
+                       head_dim, ring_capacity, status, stream);
 }
 
 }  // extern "C"

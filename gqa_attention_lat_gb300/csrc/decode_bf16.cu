@@ -78,7 +78,7 @@ struct DecodeCfg {
 struct StageRec {
     int b, hk, hb;      // unit
     int key0;           // cache row of the tile's first key
-    int ke;             // end (exclusive) of the piece's keys
+    int ke;             // end (exclusive) of the cache rows of the tile's part of the unit
     int first, last;    // first / last tile of the piece
     int kq;             // piece number within this CTA (selects the query buffer)
     int slot, nseg;     // partial slot of the piece, pieces of the unit
@@ -92,19 +92,33 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c, int rows) {
     return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-struct SeqKeys {  // visible keys of one sequence
-    int lo, n;
+// Visible keys of one sequence as cache rows: n1 rows from row s1, then (a ring cache
+// that wrapped) n2 rows from row 0.  Each part is tiled separately, so no tile crosses
+// the end of the ring.
+struct SeqKeys {
+    int s1, n1, n2, n;
 };
 __device__ __forceinline__ SeqKeys seq_keys_of(const DecodeArgs &a, int kv_len) {
     SeqKeys s;
     if (kv_len < 0 || kv_len > a.max_kv_len) {  // reported once, by CTA 0
-        s.lo = 0;
-        s.n = 0;
+        s.s1 = s.n1 = s.n2 = s.n = 0;
         return s;
     }
-    s.lo = a.window > 0 ? max(0, kv_len - a.window) : 0;
-    s.n = kv_len - s.lo;
+    const int lo = a.window > 0 ? max(0, kv_len - a.window) : 0;
+    s.n = kv_len - lo;
+    if (a.ring > 0) {
+        s.s1 = lo % a.ring;
+        s.n1 = min(s.n, a.ring - s.s1);
+    } else {
+        s.s1 = lo;
+        s.n1 = s.n;
+    }
+    s.n2 = s.n - s.n1;
     return s;
+}
+template <int T>
+__device__ __forceinline__ int seq_tiles(const SeqKeys &s) {  // tiles of one unit
+    return (s.n1 + T - 1) / T + (s.n2 + T - 1) / T;
 }
 __device__ __forceinline__ SeqKeys seq_keys(const DecodeArgs &a, int b) {
     return seq_keys_of(a, a.kv_lens[b]);
@@ -156,7 +170,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     for (int b = b_lo; b < b_hi; ++b) {
         const int kv_len = a.kv_lens[b];
         const SeqKeys sk = seq_keys_of(a, kv_len);
-        my_sum += (long long)((sk.n + T - 1) / T) * HU;
+        my_sum += (long long)seq_tiles<T>(sk) * HU;
         if (blockIdx.x == 0) {  // CTA 0 handles sequences with nothing to stream
             if (kv_len < 0 || kv_len > a.max_kv_len) {
                 report_status(a.status, kErrBounds);
@@ -191,7 +205,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
         long long p = my_start;
         for (int b = b_lo; b < b_hi; ++b) {
             const SeqKeys sk = seq_keys(a, b);
-            const long long w = (long long)((sk.n + T - 1) / T) * HU;
+            const long long w = (long long)seq_tiles<T>(sk) * HU;
             if (r0 >= p && r0 < p + w) {
                 *start_b = b;
                 *start_p = p;
@@ -233,7 +247,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                 SeqKeys sk = seq_keys(a, b);
                 int next_len = b + 1 < a.batch ? a.kv_lens[b + 1] : 0;  // fetched ahead
                 while (pos < r1 && ok) {
-                    const int nt = (sk.n + T - 1) / T;
+                    const int nt = seq_tiles<T>(sk);
                     const long long w = (long long)nt * HU;
                     if (pos >= pb + w) {  // nothing (left) of this sequence in our share
                         pb += w;
@@ -262,9 +276,11 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                     for (int c = 0; c < C::kCols64; ++c)
                         tma_load_3d(sQ + qs * C::kQBytes + c * kHeadsPerBlock * 128, &a.tm_q,
                                     &q_full[qs], c * 64, h0, b);
-                    const int kbeg = sk.lo + t0 * T;
-                    const int kend = sk.lo + min(sk.n, t1 * T);
-                    for (int key0 = kbeg; key0 < kend; key0 += T) {
+                    const int nt1 = (sk.n1 + T - 1) / T;  // tiles of the first part
+                    for (int t = t0; t < t1; ++t) {
+                        // cache row of the tile's first key and the end of its part
+                        const int key0 = t < nt1 ? sk.s1 + t * T : (t - nt1) * T;
+                        const int kend = t < nt1 ? sk.s1 + sk.n1 : sk.n2;
                         const int s = tg % C::kStages;
                         if (!mbar_wait_bounded(&empty[s], ((tg / C::kStages) & 1) ^ 1, abort_flag,
                                                deadline)) {
@@ -273,7 +289,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                         }
                         StageRec r;
                         r.b = b; r.hk = hk; r.hb = hb; r.key0 = key0; r.ke = kend;
-                        r.first = key0 == kbeg; r.last = key0 + T >= kend;
+                        r.first = t == t0; r.last = t == t1 - 1;
                         r.kq = kq; r.slot = slot; r.nseg = nseg; r.end = 0; r.pad = 0;
                         rec[s] = r;
                         mbar_arrive_expect_tx(&full[s], C::kStageBytes);

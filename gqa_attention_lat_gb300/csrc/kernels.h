@@ -17,6 +17,7 @@ struct AppendArgs {
     int64_t cache_rs, cache_head, cache_seq, new_rs;  // element strides
     const int32_t *pos;
     int capacity, n_new, batch, n_kv_heads, head_dim, elem_bytes;
+    int ring;                         // > 0: position p lives in slot p % ring (no bounds)
     int32_t *status;
 };
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t s);
@@ -38,6 +39,7 @@ struct RowAttnArgs {
     float softcap;                 // > 0: score s becomes softcap * tanh(s / softcap)
     const int32_t *kv_lens;
     int max_kv_len;
+    int ring;                      // > 0: key j sits in row j % ring of its sequence
     int32_t *status;
 };
 cudaError_t launch_row_attention_f32(const RowAttnArgs &a, cudaStream_t s);
@@ -56,6 +58,7 @@ struct DecodeArgs {
     int64_t out_rs;
     float *lse;
     int batch, n_heads, n_kv_heads, head_dim, window;
+    int ring;           // > 0: ring cache of `ring` rows, key j in row j % ring (window <= ring)
     float scale_log2;   // scale * log2(e): scores are exponentiated with exp2
     float cap_log2, raw_over_cap;  // score cap, as in PrefillTcArgs (cap_log2 0: none)
     // split-KV scratch: partial outputs, partial lse and arrival counters

@@ -4,6 +4,7 @@
 // "slice_set" cache append of the hf2q "Current Inference Path" page (sections 1 and 3)
 // and the kv_cache_write step of the hf2q target page (section 6.1, step 6, whose note
 // is that the stride arithmetic must match exactly).  Pure copy, one CTA per new row.
+// A ring cache (sliding-window layers) stores position p in slot p % ring instead.
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -16,7 +17,7 @@ __global__ void __launch_bounds__(128) kv_append_kernel(AppendArgs a) {
     const int p = a.pos[b];
     // A sequence whose rows fall outside the cache is skipped whole (every CTA of the
     // sequence sees the same pos[b], so none of its rows is written).
-    if (p < 0 || (int64_t)p + a.n_new > (int64_t)a.capacity) {
+    if (p < 0 || (a.ring == 0 && (int64_t)p + a.n_new > (int64_t)a.capacity)) {
         if (t == 0 && threadIdx.x == 0) report_status(a.status, kErrBounds);
         return;
     }
@@ -24,7 +25,8 @@ __global__ void __launch_bounds__(128) kv_append_kernel(AppendArgs a) {
     const int units_per_head = (int)((int64_t)a.head_dim * eb / (int64_t)sizeof(U));
     const int total = units_per_head * a.n_kv_heads;
     const int64_t src_row = ((int64_t)b * a.n_new + t) * a.new_rs;
-    const int64_t dst_row = (int64_t)b * a.cache_seq + (int64_t)(p + t) * a.cache_rs;
+    const int64_t slot = a.ring > 0 ? ((int64_t)p + t) % a.ring : (int64_t)p + t;
+    const int64_t dst_row = (int64_t)b * a.cache_seq + slot * a.cache_rs;
     for (int u = threadIdx.x; u < total; u += blockDim.x) {
         const int hk = u / units_per_head, w = u % units_per_head;
         const int64_t src = (src_row + (int64_t)hk * a.head_dim) * eb;

@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
     const float *vb = a.v + (int64_t)b * a.v_seq + (int64_t)hk * a.v_head;
     float m = -INFINITY, l = 0.f;
     for (int j = lo; j < hi; ++j) {
-        const float *kr = kb + (int64_t)j * a.k_row;
+        const int64_t jr = a.ring > 0 ? j % a.ring : j;  // ring cache slot
+        const float *kr = kb + jr * a.k_row;
         float part = 0.f;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
         const float corr = expf(m - m_new);
         const float w = expf(s - m_new);
         l = l * corr + w;
-        const float *vr = vb + (int64_t)j * a.v_row;
+        const float *vr = vb + jr * a.v_row;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const int d = lane + 32 * t;

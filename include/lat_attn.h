@@ -198,6 +198,27 @@ lat_status lat_attn_decode_softcap(lat_dtype dt, const void *q, int64_t q_rs,
                                    int32_t *status, void *stream);
 
 /*
+ * lat_attn_decode_ring — lat_attn_decode over a ring cache for sliding-window layers: each
+ * sequence's cache holds ring_capacity rows and the key at absolute position j sits in
+ * row j % ring_capacity (the cache keeps the last ring_capacity positions).  kv_lens are
+ * absolute lengths (they may exceed ring_capacity) and the visible keys are the last
+ * `window` positions, which may wrap past the end of the ring: the cache-offset case
+ * the hf2q pages flag for sliding layers (Current Inference Path, section 2 step 1:
+ * sliding window 1024; Target Architecture, section 3.3 per-layer caches).
+ * Requires 0 < window <= ring_capacity, else LAT_ERR_INVALID_ARG; size the workspace with
+ * lat_attn_decode_workspace_size(..., max_kv_len = ring_capacity).  Rows of the ring
+ * outside the window never reach the result.  All other rules are lat_attn_decode's.
+ */
+lat_status lat_attn_decode_ring(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
+                                const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,
+                                int64_t cache_seq_stride, int ring_capacity,
+                                const int32_t *kv_lens, int max_kv_len, void *out,
+                                int64_t out_rs, float *lse, int batch, int n_heads,
+                                int n_kv_heads, int head_dim, int window, float scale,
+                                void *workspace, size_t workspace_bytes, int32_t *status,
+                                void *stream);
+
+/*
  * lat_attn_decode_static — lat_attn_decode without a caller workspace.  The pages have
  * no counterpart to this call; it exists for callers that cannot allocate device
  * memory: code running inside a host framework that owns all device memory, plugins
@@ -243,6 +264,18 @@ lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cac
                          const void *k_new, const void *v_new, int64_t new_rs,
                          const int32_t *pos, int n_new, int batch, int n_kv_heads,
                          int head_dim, int32_t *status, void *stream);
+
+/*
+ * lat_kv_append_ring — lat_kv_append into a ring cache: new row t of sequence b goes to
+ * row (pos[b] + t) % ring_capacity (positions are absolute and never out of range).
+ * n_new must not exceed ring_capacity (rows would overwrite each other), else
+ * LAT_ERR_INVALID_ARG; pos[b] < 0 sets *status = LAT_ERR_BOUNDS and skips the sequence.
+ */
+lat_status lat_kv_append_ring(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
+                              int64_t cache_head_stride, int64_t cache_seq_stride,
+                              int ring_capacity, const void *k_new, const void *v_new,
+                              int64_t new_rs, const int32_t *pos, int n_new, int batch,
+                              int n_kv_heads, int head_dim, int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

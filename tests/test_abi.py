@@ -135,6 +135,26 @@ def test_softcap_must_be_finite_and_non_negative(lib, cap):
     assert e.value.status == binding.LAT_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("window,ring,code", [
+    (0, 256, binding.LAT_ERR_INVALID_ARG),      # a ring needs a window
+    (300, 256, binding.LAT_ERR_INVALID_ARG),    # the window must fit in the ring
+    (100, 0, binding.LAT_ERR_INVALID_ARG),      # no ring
+])
+def test_ring_decode_rejects_on_host(lib, window, ring, code):
+    with pytest.raises(binding.LatError) as e:
+        binding.lat_attn_decode_ring(LAT_BF16, FAKE, 4096, FAKE, FAKE, 1024, 128, 256 * 1024,
+                                     ring, FAKE, 100000, FAKE, 4096, None, 32, 32, 8, 128,
+                                     window, 0.088, FAKE, 1 << 30)
+    assert e.value.status == code
+
+
+def test_ring_append_rejects_more_rows_than_the_ring(lib):
+    with pytest.raises(binding.LatError) as e:
+        binding.lat_kv_append_ring(LAT_BF16, FAKE, FAKE, 1024, 128, 64 * 1024, 64, FAKE, FAKE,
+                                   1024, FAKE, 65, 2, 8, 128)
+    assert e.value.status == binding.LAT_ERR_INVALID_ARG
+
+
 def _prefill_cached(**kw):
     args = dict(dt=LAT_BF16, q=FAKE, q_rs=1024, k_cache=FAKE, v_cache=FAKE, cache_rs=512,
                 cache_head_stride=128, cache_seq_stride=512 * 4096, out=FAKE, out_rs=1024,

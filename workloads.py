@@ -156,6 +156,18 @@ def decode_inputs(B, Hq, Hkv, D, cap, *, kv_lens=None, dtype="bf16", device="cpu
     return DecodeInputs(q, kc, vc, lens.to(device), B, Hq, Hkv, D, cap, dtype)
 
 
+def ring_decode_inputs(B, Hq, Hkv, D, ring, max_len, *, dtype="bf16", device="cpu",
+                       seed=BASE_SEED) -> DecodeInputs:
+    """Decode inputs over a ring cache of `ring` rows per sequence (every row holds some
+    earlier position, so none is NaN); lengths are absolute, uniform in [1, max_len]."""
+    lens = torch.randint(1, max_len + 1, (B,), generator=_gen("cpu", seed, "kv_len"),
+                         dtype=torch.int64).to(torch.int32)
+    q = normal((B, Hq * D), dtype=dtype, device=device, seed=seed, role="q")
+    kc = normal((B, ring, Hkv * D), dtype=dtype, device=device, seed=seed, role="k")
+    vc = normal((B, ring, Hkv * D), dtype=dtype, device=device, seed=seed, role="v")
+    return DecodeInputs(q, kc, vc, lens.to(device), B, Hq, Hkv, D, ring, dtype)
+
+
 def sample_rows(n_rows_total: int, S: int, *, extra=(), n_random=256, seed=BASE_SEED):
     """A deterministic subset of query rows (flattened b*S + i) for large workloads:
     the first and last 4 rows of each sequence, the listed in-sequence positions
@@ -190,6 +202,8 @@ class Workload:
     L: int = 0            # prefill key length (>= S) / decode cache capacity
     cap: int = 0          # prefill_cached: cache capacity (rows per sequence)
     softcap: float = 0.0  # > 0: Gemma 2 score cap softcap * tanh(s / softcap)
+    ring: int = 0         # decode: > 0, a ring cache of L = ring rows; lengths up to max_len
+    max_len: int = 0
     causal: bool = True
     window: int = 0
     packed: bool = False
@@ -224,6 +238,10 @@ WORKLOADS = {
     # Gemma-2-shaped global layer with its attention score cap of 50
     "gemma2_softcap_prefill": Workload("gemma2_softcap_prefill", "prefill", "bf16", 1, 16, 8,
                                        256, S=8192, L=8192, softcap=50.0),
+    # Gemma-4 sliding layer decode over a 1024-row ring cache, absolute lengths up to 32768
+    "gemma4_sliding_decode_ring": Workload("gemma4_sliding_decode_ring", "decode", "bf16", 32,
+                                           16, 8, 256, L=1024, window=1024, ring=1024,
+                                           max_len=32768),
     # chunked prefill against the decode cache: 512 new rows after 1536 cached keys, read
     # from a token-major 4096-slot cache (Qwen3-0.6B attention shape)
     "qwen3_chunked_prefill": Workload("qwen3_chunked_prefill", "prefill_cached", "bf16", 8, 16,
