@@ -277,6 +277,49 @@ class PrefillCachedStep:
             raise RuntimeError("device status %s" % self.b.lat_status_string(st))
 
 
+class ProducerStep:
+    """Q/K RMS norm + RoPE + V + cache append for S new rows per sequence from a fused
+    QKV buffer (positions 0 .. S-1), into a token-major cache of `cap` slots."""
+
+    def __init__(self, wl, device):
+        from gqa_attention_lat_gb300 import binding
+        self.b = binding
+        self.wl = wl
+        width = (wl.Hq + 2 * wl.Hkv) * wl.D
+        self.qkv = W.normal((wl.B * wl.S, width), dtype=wl.dtype, device=device,
+                            seed=W.BASE_SEED, role="new")
+        self.q_w = W.normal((wl.D,), dtype=wl.dtype, device=device, seed=W.BASE_SEED, role="q")
+        self.k_w = W.normal((wl.D,), dtype=wl.dtype, device=device, seed=W.BASE_SEED, role="k")
+        tdt = W.torch_dtype(wl.dtype)
+        self.k_cache = torch.zeros((wl.B, wl.cap, wl.Hkv * wl.D), dtype=tdt, device=device)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.q_out = torch.empty((wl.B * wl.S, wl.Hq * wl.D), dtype=tdt, device=device)
+        self.pos = torch.zeros(wl.B, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.dt = binding.LAT_BF16 if wl.dtype == "bf16" else binding.LAT_F32
+        self.out = self.q_out
+
+    def __call__(self, qkv=None):
+        wl = self.wl
+        qkv = self.qkv if qkv is None else qkv
+        self.b.lat_qkv_norm_rope_append(self.dt, qkv, self.qkv.stride(0), self.q_w, self.k_w,
+                                        1e-6, 1e6, False, self.q_out, self.q_out.stride(0),
+                                        self.k_cache, self.v_cache, wl.Hkv * wl.D, wl.D,
+                                        wl.cap * wl.Hkv * wl.D, wl.cap, self.pos, wl.S, wl.B,
+                                        wl.Hq, wl.Hkv, wl.D, self.status)
+
+    def check_status(self):
+        st = int(self.status.item())
+        if st != 0:
+            raise RuntimeError("device status %s" % self.b.lat_status_string(st))
+
+
+def producer_bytes(wl):
+    es = 2 if wl.dtype == "bf16" else 4
+    rows = wl.B * wl.S
+    return float(rows * (wl.Hq + 2 * wl.Hkv) * wl.D * es * 2 + 2 * wl.D * es)  # read + write
+
+
 class DecodeStep:
     def __init__(self, wl, device):
         from gqa_attention_lat_gb300 import binding
@@ -354,6 +397,20 @@ def measure_extra(device, flush, stream, peaks, reps=10):
                      "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "gflop": flops / 1e9}
         del step
         torch.cuda.empty_cache()
+    for name in ("qwen3_qkv_producer",):
+        wl = W.WORKLOADS[name]
+        step = ProducerStep(wl, device)
+        for _ in range(3):
+            step()
+        ms = time_steps(step, reps, flush, stream)
+        step.check_status()
+        bytes_ = producer_bytes(wl)
+        t = statistics.median(ms) / 1e3
+        res[name] = {"kind": "producer", "ms": statistics.median(ms), "gbs": bytes_ / t / 1e9,
+                     "bound": "hbm", "frac_of_hbm_peak": bytes_ / t / 1e9 / peaks["hbm_gbs"],
+                     "mbytes": bytes_ / 1e6}
+        del step
+        torch.cuda.empty_cache()
     for name in ("decode_b32_h32_kv8_d128", "gemma4_global_decode", "gemma4_sliding_decode_ring"):
         wl = W.WORKLOADS[name]
         step = DecodeStep(wl, device)
@@ -386,6 +443,9 @@ def e2e_measure(step, steps, stream):
         d = step.di
         parents = [step.q, d.k_cache, d.v_cache]
         outs = [step.out, step.lse]
+    elif isinstance(step, ProducerStep):
+        parents = [step.qkv]
+        outs = [step.q_out]  # the cache rows stay on the device for the attention kernels
     else:
         d = step.di
         parents = [d.q, d.k_cache, d.v_cache, d.kv_lens]
@@ -501,6 +561,14 @@ def workload_config(wl):
             "batch": wl.B, "kv_capacity": wl.L, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
             "head_dim": wl.D, "window": wl.window,
             "l2": L2_NOTE, "parallelism": "replicas"}
+    if wl.kind == "producer":
+        return {"workload": "%s: Q/K RMS norm + neox RoPE + cache append, %d rows of a fused "
+                            "QKV [%d, %d], Hq%d Hkv%d D%d, token-major cache %d slots %s" % (
+                                wl.name, wl.B * wl.S, wl.B * wl.S,
+                                (wl.Hq + 2 * wl.Hkv) * wl.D, wl.Hq, wl.Hkv, wl.D, wl.cap,
+                                wl.dtype),
+                "batch": wl.B, "seq_len": wl.S, "n_heads": wl.Hq, "n_kv_heads": wl.Hkv,
+                "head_dim": wl.D, "l2": L2_NOTE, "parallelism": "replicas"}
     where = ""
     if wl.packed:
         where = ", packed QKV [%d, %d]" % (wl.B * wl.S, (wl.Hq + 2 * wl.Hkv) * wl.D)
@@ -564,7 +632,7 @@ def main():
         raise SystemExit("bench workloads are bf16 (the fp32 shapes are parity cases)")
     flush = Flusher(device)
     step = {"prefill": PrefillStep, "prefill_cached": PrefillCachedStep,
-            "decode": DecodeStep}[wl.kind](wl, device)
+            "decode": DecodeStep, "producer": ProducerStep}[wl.kind](wl, device)
     sampler = ClockSampler(local)
     sampler.start()
     for _ in range(args.warmup):
@@ -589,6 +657,12 @@ def main():
         ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
         bound = "hbm" if intensity < ridge else "tensor"
         profile, srcs = "prefill_tc_%s.md" % wl.name, ["prefill_tc.cu", "device_common.cuh", "kernels.h"]
+    elif wl.kind == "producer":
+        flops, alg_bytes = 0.0, producer_bytes(wl)
+        unit, work = "GB/s", alg_bytes / 1e9
+        kernel = "qkv_producer_fast<%d>" % wl.D
+        bound = "hbm"
+        profile, srcs = "qkv_producer_%s.md" % wl.name, ["qkv_producer.cu", "device_common.cuh", "kernels.h"]
     else:
         flops, alg_bytes, _ = decode_work(wl, step.di.kv_lens.cpu().tolist())
         unit, work = "GB/s", alg_bytes / 1e9

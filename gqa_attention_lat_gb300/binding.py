@@ -52,6 +52,9 @@ _SIGNATURES = {
                                     _P, _P]),
     "lat_kv_append_ring": (_I32, [_I32, _P, _P, _I64, _I64, _I64, _I32, _P, _P, _I64, _P, _I32,
                                   _I32, _I32, _I32, _P, _P]),
+    "lat_qkv_norm_rope_append": (_I32, [_I32, _P, _I64, _P, _P, _F32, ctypes.c_double, _I32,
+                                        _P, _I64, _P, _P, _I64, _I64, _I64, _I32, _P, _I32,
+                                        _I32, _I32, _I32, _I32, _P, _P]),
     "lat_attn_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "lat_attn_decode": (_I32, [_I32, _P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _I64,
                                _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _P]),
@@ -154,6 +157,17 @@ def lat_kv_append_ring(dt, k_cache, v_cache, cache_rs, cache_head_stride, cache_
         dt, _ptr(k_cache), _ptr(v_cache), cache_rs, cache_head_stride, cache_seq_stride,
         ring_capacity, _ptr(k_new), _ptr(v_new), new_rs, _ptr(pos), n_new, batch, n_kv_heads,
         head_dim, _ptr(status), _stream(stream)), "lat_kv_append_ring")
+
+
+def lat_qkv_norm_rope_append(dt, qkv, qkv_rs, q_norm_w, k_norm_w, eps, rope_base, v_unit_norm,
+                             q_out, q_out_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                             cache_seq_stride, capacity, pos, n_new, batch, n_heads, n_kv_heads,
+                             head_dim, status=None, stream=None):
+    _check(library().lat_qkv_norm_rope_append(
+        dt, _ptr(qkv), qkv_rs, _ptr(q_norm_w), _ptr(k_norm_w), eps, rope_base,
+        int(bool(v_unit_norm)), _ptr(q_out), q_out_rs, _ptr(k_cache), _ptr(v_cache), cache_rs,
+        cache_head_stride, cache_seq_stride, capacity, _ptr(pos), n_new, batch, n_heads,
+        n_kv_heads, head_dim, _ptr(status), _stream(stream)), "lat_qkv_norm_rope_append")
 
 
 def lat_attn_prefill_cached(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,

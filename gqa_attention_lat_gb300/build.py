@@ -22,7 +22,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblat_attn.so")
 
 SOURCES = ["api.cu", "kv_append.cu", "row_attention_f32.cu", "decode_bf16.cu", "prefill_tc.cu",
-           "decode_static.cu"]
+           "decode_static.cu", "qkv_producer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                  "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -491,6 +491,57 @@ lat_status lat_kv_append(lat_dtype dt, void *k_cache, void *v_cache, int64_t cac
                        0, status, stream);
 }
 
+lat_status lat_qkv_norm_rope_append(lat_dtype dt, const void *qkv, int64_t qkv_rs,
+                                    const void *q_norm_w, const void *k_norm_w, float eps,
+                                    double rope_base, int v_unit_norm, void *q_out,
+                                    int64_t q_out_rs, void *k_cache, void *v_cache,
+                                    int64_t cache_rs, int64_t cache_head_stride,
+                                    int64_t cache_seq_stride, int capacity, const int32_t *pos,
+                                    int n_new, int batch, int n_heads, int n_kv_heads,
+                                    int head_dim, int32_t *status, void *stream) {
+    if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
+    if (batch < 0 || n_new < 0 || capacity < 0 || n_heads <= 0 || n_kv_heads <= 0 ||
+        n_heads % n_kv_heads != 0)
+        return LAT_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return LAT_ERR_UNSUPPORTED;
+    if (!(eps >= 0.f) || !isfinite(eps) || !(rope_base > 1.0) || !isfinite(rope_base))
+        return LAT_ERR_INVALID_ARG;
+    if (batch == 0 || n_new == 0) return LAT_OK;
+    if (!qkv || !q_out || !k_cache || !v_cache || !pos) return LAT_ERR_INVALID_ARG;
+    if (qkv_rs < (int64_t)(n_heads + 2 * n_kv_heads) * head_dim ||
+        q_out_rs < (int64_t)n_heads * head_dim || cache_rs <= 0 || cache_head_stride <= 0 ||
+        cache_seq_stride <= 0)
+        return LAT_ERR_INVALID_ARG;
+    lat::ProducerArgs a{};
+    a.qkv = qkv;
+    a.qkv_rs = qkv_rs;
+    a.q_w = q_norm_w;
+    a.k_w = k_norm_w;
+    a.eps = eps;
+    a.v_unit_norm = v_unit_norm != 0;
+    a.q_out = q_out;
+    a.q_out_rs = q_out_rs;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.cache_rs = cache_rs;
+    a.cache_head = cache_head_stride;
+    a.cache_seq = cache_seq_stride;
+    a.capacity = capacity;
+    a.pos = pos;
+    a.n_new = n_new;
+    a.batch = batch;
+    a.n_heads = n_heads;
+    a.n_kv_heads = n_kv_heads;
+    a.head_dim = head_dim;
+    a.status = status;
+    for (int i = 0; i < head_dim / 2; ++i)  // the rotation frequencies, in double
+        a.inv_freq[i] = pow(rope_base, -2.0 * i / head_dim);
+    return lat::launch_qkv_producer(a, dt == LAT_BF16, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? LAT_OK
+               : LAT_ERR_CUDA;
+}
+
 lat_status lat_kv_append_ring(lat_dtype dt, void *k_cache, void *v_cache, int64_t cache_rs,
                               int64_t cache_head_stride, int64_t cache_seq_stride,
                               int ring_capacity, const void *k_new, const void *v_new,

@@ -22,6 +22,26 @@ struct AppendArgs {
 };
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t s);
 
+// ---------------------------------------------------------------- attention-input producer
+// Q/K RMS norm + neox RoPE + V (copy or unit norm) + cache append, one CTA per new row.
+struct ProducerArgs {
+    const void *qkv;                 // [batch * n_new rows, qkv_rs]: Q heads, K heads, V heads
+    int64_t qkv_rs;
+    const void *q_w, *k_w;           // [head_dim] norm weights (nullable: weight 1)
+    float eps;
+    int v_unit_norm;
+    void *q_out;                     // [batch * n_new rows, q_out_rs]
+    int64_t q_out_rs;
+    void *k_cache, *v_cache;
+    int64_t cache_rs, cache_head, cache_seq;
+    int capacity;
+    const int32_t *pos;
+    int n_new, batch, n_heads, n_kv_heads, head_dim;
+    int32_t *status;
+    double inv_freq[256];            // base^(-2i/D), i < head_dim/2, from the host in double
+};
+cudaError_t launch_qkv_producer(const ProducerArgs &a, bool bf16, cudaStream_t s);
+
 // ---------------------------------------------------------------- fp32 row kernel
 // One warp per (query row, query head); used for every fp32 prefill and decode.
 // Element (b, j, hk, d) of K is k[b*k_seq + j*k_row + hk*k_head + d] (V alike);

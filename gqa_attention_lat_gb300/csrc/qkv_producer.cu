@@ -1,0 +1,265 @@
+// qkv_producer.cu — the steps right before attention, fused: Q/K RMS norm, rotary position
+// embedding, V (unit norm or copy), and the KV-cache append.
+//
+// What it computes, for new row t of sequence b at absolute position p = pos[b] + t
+// (the hf2q "Current Inference Path" page, section 3: Q norm and K norm (RmsNorm), V unit
+// norm, RoPE apply, KV cache append; the lattice-inference DESIGN page's
+// fused_qk_norm_rope: one RMS norm over head_dim, then head_dim/2 rotation pairs):
+//   Q and K heads:  y = x / sqrt(mean(x^2) + eps) * w        (w the head-dim norm weight)
+//                   element i < D/2 pairs with i + D/2 and both rotate by
+//                   theta_i = p * base^(-2i/D)  (the neox pairing the hf2q page names)
+//   V heads:        copied, or x / sqrt(mean(x^2) + eps) when unit-normed (Gemma 4)
+// Q goes to q_out (the attention input); K and V go to cache row p.
+//
+// How: one CTA per new row (two forms, below: a vectorised one for head_dim 64/128/256 and
+// 16-byte aligned rows, and a general one).  Its threads first turn the row's position into cos/sin of
+// every rotation angle, in shared memory: p * base^(-2i/D) is formed in double precision
+// (the host passes the inverse frequencies in double) and reduced by 2*pi there, so the
+// fp32 sine and cosine see an argument below pi even at positions in the hundreds of
+// thousands.  Then each warp takes one head at a time: a warp-shuffle sum of squares,
+// the scaled row staged in shared memory, and each lane writes the rotated elements it
+// owns.  fp32 arithmetic throughout, one rounding to the output type.
+#include <math.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace lat {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr double kTwoPi = 6.283185307179586;
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) qkv_producer_kernel(const __grid_constant__ ProducerArgs a) {
+    extern __shared__ float smem[];
+    const int D = a.head_dim, half = D / 2;
+    float *cs = smem;                 // [half] cos
+    float *sn = smem + half;          // [half] sin
+    float *stage = smem + 2 * half;   // [kWarps][D] normed rows
+    const int row = blockIdx.x;
+    const int b = row / a.n_new, t = row % a.n_new;
+    const int p0 = a.pos[b];
+    // a sequence whose rows fall outside the cache is skipped whole (every CTA of the
+    // sequence sees the same pos[b]), like the plain append
+    if (p0 < 0 || (int64_t)p0 + a.n_new > (int64_t)a.capacity) {
+        if (t == 0 && threadIdx.x == 0) report_status(a.status, kErrBounds);
+        return;
+    }
+    const int p = p0 + t;
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        double th = (double)p * a.inv_freq[i];
+        th -= rint(th * (1.0 / kTwoPi)) * kTwoPi;
+        float s, c;
+        sincosf((float)th, &s, &c);
+        cs[i] = c;
+        sn[i] = s;
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *st = stage + warp * D;
+    const T *src_row = static_cast<const T *>(a.qkv) + ((int64_t)b * a.n_new + t) * a.qkv_rs;
+    const int n_q = a.n_heads, n_k = a.n_kv_heads;
+    const int total = n_q + 2 * n_k;
+    for (int hh = warp; hh < total; hh += kWarps) {
+        const T *x = src_row + (int64_t)hh * D;
+        const bool is_q = hh < n_q, is_k = !is_q && hh < n_q + n_k, is_v = hh >= n_q + n_k;
+        float ss = 0.f;
+        for (int e = lane; e < D; e += 32) {
+            const float v = to_f<T>(x[e]);
+            st[e] = v;
+            ss = fmaf(v, v, ss);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const bool normed = !is_v || a.v_unit_norm;
+        const float r = normed ? 1.f / sqrtf(ss / (float)D + a.eps) : 1.f;
+        const T *w = is_q ? static_cast<const T *>(a.q_w) : (is_k ? static_cast<const T *>(a.k_w) : nullptr);
+        __syncwarp();
+        for (int e = lane; e < D; e += 32) st[e] = st[e] * r * (w != nullptr ? to_f<T>(w[e]) : 1.f);
+        __syncwarp();
+        T *dst;
+        if (is_q) {
+            dst = static_cast<T *>(a.q_out) + ((int64_t)b * a.n_new + t) * a.q_out_rs + (int64_t)hh * D;
+        } else {
+            const int hk = is_k ? hh - n_q : hh - n_q - n_k;
+            T *cache = static_cast<T *>(is_k ? a.k_cache : a.v_cache);
+            dst = cache + (int64_t)b * a.cache_seq + (int64_t)p * a.cache_rs + (int64_t)hk * a.cache_head;
+        }
+        if (is_v) {
+            for (int e = lane; e < D; e += 32) dst[e] = from_f<T>(st[e]);
+        } else {  // rotation pair (i, i + D/2)
+            for (int i = lane; i < half; i += 32) {
+                const float x0 = st[i], x1 = st[i + half], c = cs[i], sv = sn[i];
+                dst[i] = from_f<T>(x0 * c - x1 * sv);
+                dst[i + half] = from_f<T>(x0 * sv + x1 * c);
+            }
+        }
+        __syncwarp();  // the stage is rewritten by the next head
+    }
+}
+
+// 8 consecutive elements <-> registers, as 16-byte accesses
+template <typename T>
+__device__ __forceinline__ void load8(const T *p, float v[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float v[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float *p, float v[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <typename T>
+__device__ __forceinline__ void store8(T *p, const float v[8]);
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *p, const float v[8]) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+template <>
+__device__ __forceinline__ void store8<float>(float *p, const float v[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Vectorised form for head_dim 64/128/256: a head is D/8 lanes of 8 consecutive elements
+// (16-byte loads and stores), a warp holds 32/(D/8) heads at once, the sum of squares is
+// a shuffle reduction inside each head's lanes, and the rotation partner of lane j
+// (elements 8j..8j+7 of the first half) is lane j + D/16 of the same head.
+constexpr int kFastWarps = 8;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kFastWarps * 32, 8) qkv_producer_fast(const __grid_constant__ ProducerArgs a) {
+    constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2;
+    __shared__ float cs[HALF], sn[HALF];
+    const int row = blockIdx.x;
+    const int b = row / a.n_new, t = row % a.n_new;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane / LPH, j = lane % LPH;
+    const T *src_row = static_cast<const T *>(a.qkv) + ((int64_t)b * a.n_new + t) * a.qkv_rs;
+    const int n_q = a.n_heads, n_k = a.n_kv_heads, total = n_q + 2 * n_k;
+    // The first pass's head rows do not depend on the position: their loads are in flight
+    // while the rotation table is built.
+    float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int base = warp * HPW;
+    if (base + sub < total) load8<T>(src_row + (int64_t)(base + sub) * D + 8 * j, x);
+    const int p0 = a.pos[b];
+    if (p0 < 0 || (int64_t)p0 + a.n_new > (int64_t)a.capacity) {  // skipped whole
+        if (t == 0 && threadIdx.x == 0) report_status(a.status, kErrBounds);
+        return;
+    }
+    const int p = p0 + t;
+    for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
+        double th = (double)p * a.inv_freq[i];
+        th -= rint(th * (1.0 / kTwoPi)) * kTwoPi;
+        float s, c;
+        __sincosf((float)th, &s, &c);  // |th| <= pi: the hardware form is accurate to ~2^-21
+        cs[i] = c;
+        sn[i] = s;
+    }
+    __syncthreads();
+    const bool first_half = j < LPH / 2;
+    const int i0 = 8 * (first_half ? j : j - LPH / 2);  // rotation index of element 0
+    for (bool first = true; base < total; base += kFastWarps * HPW, first = false) {  // warp-uniform
+        const int hh = base + sub;
+        const bool live = hh < total;
+        const bool is_q = hh < n_q, is_k = !is_q && hh < n_q + n_k, is_v = hh >= n_q + n_k;
+        if (!first) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = 0.f;
+            if (live) load8<T>(src_row + (int64_t)hh * D + 8 * j, x);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
+#pragma unroll
+        for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const bool normed = !is_v || a.v_unit_norm;
+        const float r = normed ? rsqrtf(fmaf(ss, 1.f / (float)D, a.eps)) : 1.f;
+        const T *w = is_q ? static_cast<const T *>(a.q_w) : (is_k ? static_cast<const T *>(a.k_w) : nullptr);
+        float wv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if (live && w != nullptr) load8<T>(w + 8 * j, wv);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] *= r * wv[k];
+        float px[8];  // the rotation partner's elements
+#pragma unroll
+        for (int k = 0; k < 8; ++k) px[k] = __shfl_xor_sync(0xffffffffu, x[k], LPH / 2);
+        if (!live) continue;
+        if (!is_v) {
+            // first half: (a, b) -> a cos - b sin; second half: b -> a sin + b cos
+            const float sg = first_half ? -1.f : 1.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = fmaf(sg * px[k], sn[i0 + k], x[k] * cs[i0 + k]);
+        }
+        T *dst;
+        if (is_q) {
+            dst = static_cast<T *>(a.q_out) + ((int64_t)b * a.n_new + t) * a.q_out_rs + (int64_t)hh * D;
+        } else {
+            const int hk = is_k ? hh - n_q : hh - n_q - n_k;
+            T *cache = static_cast<T *>(is_k ? a.k_cache : a.v_cache);
+            dst = cache + (int64_t)b * a.cache_seq + (int64_t)p * a.cache_rs + (int64_t)hk * a.cache_head;
+        }
+        store8<T>(dst + 8 * j, x);
+    }
+}
+
+template <typename T>
+cudaError_t launch_t(const ProducerArgs &a, unsigned blocks, bool vec, cudaStream_t s) {
+    if (vec) {
+        switch (a.head_dim) {
+            case 64: qkv_producer_fast<T, 64><<<blocks, kFastWarps * 32, 0, s>>>(a); return cudaGetLastError();
+            case 128: qkv_producer_fast<T, 128><<<blocks, kFastWarps * 32, 0, s>>>(a); return cudaGetLastError();
+            case 256: qkv_producer_fast<T, 256><<<blocks, kFastWarps * 32, 0, s>>>(a); return cudaGetLastError();
+            default: break;
+        }
+    }
+    const size_t smem = (size_t)(a.head_dim + kWarps * a.head_dim) * sizeof(float);
+    qkv_producer_kernel<T><<<blocks, kWarps * 32, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+bool aligned16_all(const ProducerArgs &a, int64_t es) {
+    auto ok = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return ok(a.qkv) && ok(a.q_out) && ok(a.k_cache) && ok(a.v_cache) &&
+           (a.q_w == nullptr || ok(a.q_w)) && (a.k_w == nullptr || ok(a.k_w)) &&
+           (a.qkv_rs * es) % 16 == 0 && (a.q_out_rs * es) % 16 == 0 && (a.cache_rs * es) % 16 == 0 &&
+           (a.cache_head * es) % 16 == 0 && (a.cache_seq * es) % 16 == 0;
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_producer(const ProducerArgs &a, bool bf16, cudaStream_t s) {
+    const int64_t blocks = (int64_t)a.batch * a.n_new;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // the vectorised form needs 16-byte aligned rows; anything else takes the general one
+    const bool vec = aligned16_all(a, bf16 ? 2 : 4);
+    return bf16 ? launch_t<__nv_bfloat16>(a, (unsigned)blocks, vec, s)
+                : launch_t<float>(a, (unsigned)blocks, vec, s);
+}
+
+}  // namespace lat

@@ -277,6 +277,36 @@ lat_status lat_kv_append_ring(lat_dtype dt, void *k_cache, void *v_cache, int64_
                               int64_t new_rs, const int32_t *pos, int n_new, int batch,
                               int n_kv_heads, int head_dim, int32_t *status, void *stream);
 
+/*
+ * lat_qkv_norm_rope_append — the steps right before attention, fused for the new token
+ * rows of a fused QKV projection: Q norm and K norm (RMS norm over head_dim with a
+ * head_dim weight), rotary position embedding, V unit norm or copy, then the KV-cache
+ * append (the hf2q "Current Inference Path" page, section 3: Q norm, K norm, V unit norm,
+ * RoPE apply, KV cache append; the lattice-inference DESIGN page's fused_qk_norm_rope).
+ *
+ * For new row t of sequence b at position p = pos[b] + t, with x one head of that row:
+ *   Q, K heads:  y = x / sqrt(mean(x^2) + eps) * w   (w = q_norm_w or k_norm_w; NULL = 1)
+ *                then element i < D/2 and element i + D/2 rotate by theta_i = p *
+ *                rope_base^(-2i/D):  (a, b) -> (a cos - b sin, a sin + b cos)
+ *   V heads:     x, or x / sqrt(mean(x^2) + eps) when v_unit_norm != 0
+ * Layout: qkv row (b,t) at qkv[(b*n_new + t)*qkv_rs]: n_heads Q heads, then n_kv_heads K
+ *   heads, then n_kv_heads V heads, each head_dim wide (the packed layout of
+ *   lat_attn_prefill); q_out row (b,t) at q_out[(b*n_new + t)*q_out_rs] (n_heads heads);
+ *   caches, capacity and pos as in lat_kv_append (rows p of sequence b).  Norm weights are
+ *   head_dim elements of dtype dt.  fp32 arithmetic, one rounding to dt.
+ * eps must be finite and >= 0 and rope_base finite and > 1, else LAT_ERR_INVALID_ARG.  A
+ * sequence whose rows would fall outside [0, capacity) is skipped whole (nothing of it is
+ * written, Q included) and sets *status = LAT_ERR_BOUNDS.
+ */
+lat_status lat_qkv_norm_rope_append(lat_dtype dt, const void *qkv, int64_t qkv_rs,
+                                    const void *q_norm_w, const void *k_norm_w, float eps,
+                                    double rope_base, int v_unit_norm, void *q_out,
+                                    int64_t q_out_rs, void *k_cache, void *v_cache,
+                                    int64_t cache_rs, int64_t cache_head_stride,
+                                    int64_t cache_seq_stride, int capacity, const int32_t *pos,
+                                    int n_new, int batch, int n_heads, int n_kv_heads,
+                                    int head_dim, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

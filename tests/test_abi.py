@@ -211,6 +211,42 @@ def test_append_nothing_is_a_no_op(lib):
     _append(batch=0)
 
 
+def _producer(**kw):
+    args = dict(dt=LAT_BF16, qkv=FAKE, qkv_rs=32 * 128, q_norm_w=FAKE, k_norm_w=FAKE, eps=1e-6,
+                rope_base=1e6, v_unit_norm=False, q_out=FAKE, q_out_rs=16 * 128, k_cache=FAKE,
+                v_cache=FAKE, cache_rs=1024, cache_head_stride=128, cache_seq_stride=1024 * 64,
+                capacity=64, pos=FAKE, n_new=4, batch=2, n_heads=16, n_kv_heads=8,
+                head_dim=128)
+    args.update(kw)
+    return binding.lat_qkv_norm_rope_append(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dt=7), binding.LAT_ERR_INVALID_ARG),
+    (dict(n_heads=12, n_kv_heads=8), binding.LAT_ERR_INVALID_ARG),
+    (dict(head_dim=48), binding.LAT_ERR_UNSUPPORTED),
+    (dict(eps=-1e-6), binding.LAT_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), binding.LAT_ERR_INVALID_ARG),
+    (dict(rope_base=1.0), binding.LAT_ERR_INVALID_ARG),
+    (dict(rope_base=float("inf")), binding.LAT_ERR_INVALID_ARG),
+    (dict(qkv_rs=31 * 128), binding.LAT_ERR_INVALID_ARG),   # shorter than Hq + 2 Hkv heads
+    (dict(q_out_rs=15 * 128), binding.LAT_ERR_INVALID_ARG),
+    (dict(pos=None), binding.LAT_ERR_INVALID_ARG),
+    (dict(k_cache=None), binding.LAT_ERR_INVALID_ARG),
+    (dict(cache_rs=0), binding.LAT_ERR_INVALID_ARG),
+    (dict(batch=-1), binding.LAT_ERR_INVALID_ARG),
+])
+def test_producer_rejects_on_host(lib, kw, code):
+    with pytest.raises(binding.LatError) as e:
+        _producer(**kw)
+    assert e.value.status == code
+
+
+def test_producer_nothing_is_a_no_op(lib):
+    _producer(n_new=0)
+    _producer(batch=0)
+
+
 def test_library_is_sm103a_only():
     from gqa_attention_lat_gb300 import build
     assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

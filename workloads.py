@@ -192,7 +192,7 @@ def sample_rows(n_rows_total: int, S: int, *, extra=(), n_random=256, seed=BASE_
 @dataclass
 class Workload:
     name: str
-    kind: str             # "prefill", "prefill_cached" or "decode"
+    kind: str             # "prefill", "prefill_cached", "decode" or "producer"
     dtype: str
     B: int
     Hq: int
@@ -242,6 +242,10 @@ WORKLOADS = {
     "gemma4_sliding_decode_ring": Workload("gemma4_sliding_decode_ring", "decode", "bf16", 32,
                                            16, 8, 256, L=1024, window=1024, ring=1024,
                                            max_len=32768),
+    # the attention-input producer on the Qwen3-0.6B prefill rows: Q/K RMS norm, RoPE
+    # (base 1e6), V copy, append into a token-major 4096-slot cache
+    "qwen3_qkv_producer": Workload("qwen3_qkv_producer", "producer", "bf16", 8, 16, 8, 64,
+                                   S=512, L=512, cap=4096),
     # chunked prefill against the decode cache: 512 new rows after 1536 cached keys, read
     # from a token-major 4096-slot cache (Qwen3-0.6B attention shape)
     "qwen3_chunked_prefill": Workload("qwen3_chunked_prefill", "prefill_cached", "bf16", 8, 16,
