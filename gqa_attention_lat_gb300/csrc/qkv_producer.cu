@@ -11,14 +11,15 @@
 //   V heads:        copied, or x / sqrt(mean(x^2) + eps) when unit-normed (Gemma 4)
 // Q goes to q_out (the attention input); K and V go to cache row p.
 //
-// How: one CTA per new row (two forms, below: a vectorised one for head_dim 64/128/256 and
-// 16-byte aligned rows, and a general one).  Its threads first turn the row's position into cos/sin of
-// every rotation angle, in shared memory: p * base^(-2i/D) is formed in double precision
-// (the host passes the inverse frequencies in double) and reduced by 2*pi there, so the
-// fp32 sine and cosine see an argument below pi even at positions in the hundreds of
-// thousands.  Then each warp takes one head at a time: a warp-shuffle sum of squares,
-// the scaled row staged in shared memory, and each lane writes the rotated elements it
-// owns.  fp32 arithmetic throughout, one rounding to the output type.
+// How: one CTA per new row, in two forms (a vectorised one for head_dim 64/128/256 with
+// 16-byte aligned rows and strides, and a general one).  The row's threads turn its
+// position into cos/sin of every rotation angle, in shared memory: p * base^(-2i/D) is
+// formed in double precision (the host passes the inverse frequencies in double) and
+// reduced by 2*pi there, so the fp32 sine and cosine see an argument below pi even at
+// positions in the hundreds of thousands.  The general form then takes one head per warp
+// at a time (a warp-shuffle sum of squares, the scaled head staged in shared memory, each
+// lane writing the rotated elements it owns); the vectorised form is described at its
+// kernel.  fp32 arithmetic throughout, one rounding to the output type.
 #include <math.h>
 
 #include "device_common.cuh"
@@ -150,25 +151,102 @@ __device__ __forceinline__ void store8<float>(float *p, const float v[8]) {
 // (16-byte loads and stores), a warp holds 32/(D/8) heads at once, the sum of squares is
 // a shuffle reduction inside each head's lanes, and the rotation partner of lane j
 // (elements 8j..8j+7 of the first half) is lane j + D/16 of the same head.
+//
+// Only the rotation needs the position: the first pass's head rows, norm weights and the
+// position are all loaded up front, the norm of the first pass is done before the one
+// barrier that publishes the cos/sin table, and the rotation and the stores follow it.
 constexpr int kFastWarps = 8;
 
+// 8 elements held as raw 16-byte words until they are needed as floats (fewer registers)
+template <typename T>
+struct Raw8 {
+    static constexpr int kWords = (int)sizeof(T) / 2;  // uint4 words: 1 for bf16, 2 for fp32
+    uint4 u[kWords];
+    __device__ __forceinline__ void load(const T *p) {
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) u[i] = reinterpret_cast<const uint4 *>(p)[i];
+    }
+    __device__ __forceinline__ void fill(uint32_t bits) {
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) u[i] = make_uint4(bits, bits, bits, bits);
+    }
+    __device__ __forceinline__ float get(int k) const;
+};
+template <>
+__device__ __forceinline__ float Raw8<__nv_bfloat16>::get(int k) const {
+    const uint32_t w = k < 2 ? u[0].x : k < 4 ? u[0].y : k < 6 ? u[0].z : u[0].w;
+    return __uint_as_float((k & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+template <>
+__device__ __forceinline__ float Raw8<float>::get(int k) const {
+    const uint4 &q = u[k >> 2];
+    const int m = k & 3;
+    return __uint_as_float(m == 0 ? q.x : m == 1 ? q.y : m == 2 ? q.z : q.w);
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kFastWarps * 32, 8) qkv_producer_fast(const __grid_constant__ ProducerArgs a) {
+struct FastHead {  // one lane's 8 elements of one head, through norm and rotation
+    static constexpr int LPH = D / 8;
+    Raw8<T> xr, wr;
+    float x[8];
+
+    __device__ __forceinline__ void load(const T *row, const ProducerArgs &a, int hh, int j, bool live,
+                                         bool is_q, bool is_k) {
+        const T *wp = is_q ? static_cast<const T *>(a.q_w) : (is_k ? static_cast<const T *>(a.k_w) : nullptr);
+        xr.fill(0u);
+        wr.fill(sizeof(T) == 2 ? 0x3f803f80u : 0x3f800000u);  // 1.0
+        if (live) xr.load(row + (int64_t)hh * D + 8 * j);
+        if (live && wp != nullptr) wr.load(wp + 8 * j);
+    }
+    // x <- x / sqrt(mean(x^2) + eps) * w (or x for a V head that is not normed)
+    __device__ __forceinline__ void norm(const ProducerArgs &a, bool normed) {
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            x[k] = xr.get(k);
+            ss = fmaf(x[k], x[k], ss);
+        }
+#pragma unroll
+        for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float r = normed ? rsqrtf(fmaf(ss, 1.f / (float)D, a.eps)) : 1.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] *= r * wr.get(k);
+    }
+    // first half: (a, b) -> a cos - b sin; second half: b -> a sin + b cos, where the
+    // partner's elements come from lane j +- D/16 (all lanes take part in the shuffle)
+    __device__ __forceinline__ void rotate(const float *cs, const float *sn, int i0, bool first_half,
+                                           bool rotated) {
+        float px[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) px[k] = __shfl_xor_sync(0xffffffffu, x[k], LPH / 2);
+        if (!rotated) return;
+        const float sg = first_half ? -1.f : 1.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = fmaf(sg * px[k], sn[i0 + k], x[k] * cs[i0 + k]);
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kFastWarps * 32, 6) qkv_producer_fast(const __grid_constant__ ProducerArgs a) {
     constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2;
     __shared__ float cs[HALF], sn[HALF];
     const int row = blockIdx.x;
-    const int b = row / a.n_new, t = row % a.n_new;
+    const int b = row / a.n_new, t = row - b * a.n_new;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane / LPH, j = lane % LPH;
-    const T *src_row = static_cast<const T *>(a.qkv) + ((int64_t)b * a.n_new + t) * a.qkv_rs;
+    const T *src_row = static_cast<const T *>(a.qkv) + (int64_t)row * a.qkv_rs;
     const int n_q = a.n_heads, n_k = a.n_kv_heads, total = n_q + 2 * n_k;
-    // The first pass's head rows do not depend on the position: their loads are in flight
-    // while the rotation table is built.
-    float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int base = warp * HPW;
-    if (base + sub < total) load8<T>(src_row + (int64_t)(base + sub) * D + 8 * j, x);
+    const bool first_half = j < LPH / 2;
+    const int i0 = 8 * (first_half ? j : j - LPH / 2);  // rotation index of element 0
+
+    FastHead<T, D> h;
+    int hh = warp * HPW + sub;
+    bool live = hh < total, is_q = hh < n_q, is_k = !is_q && hh < n_q + n_k;
+    h.load(src_row, a, hh, j, live, is_q, is_k);
     const int p0 = a.pos[b];
-    if (p0 < 0 || (int64_t)p0 + a.n_new > (int64_t)a.capacity) {  // skipped whole
+    h.norm(a, is_q || is_k || a.v_unit_norm);
+    const bool skip = p0 < 0 || (int64_t)p0 + a.n_new > (int64_t)a.capacity;  // CTA-uniform
+    if (skip) {  // the sequence is skipped whole
         if (t == 0 && threadIdx.x == 0) report_status(a.status, kErrBounds);
         return;
     }
@@ -176,54 +254,30 @@ __global__ void __launch_bounds__(kFastWarps * 32, 8) qkv_producer_fast(const __
     for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
         double th = (double)p * a.inv_freq[i];
         th -= rint(th * (1.0 / kTwoPi)) * kTwoPi;
-        float s, c;
-        __sincosf((float)th, &s, &c);  // |th| <= pi: the hardware form is accurate to ~2^-21
-        cs[i] = c;
-        sn[i] = s;
+        float sv, cv;
+        __sincosf((float)th, &sv, &cv);  // |th| <= pi: the hardware form is accurate to ~2^-21
+        cs[i] = cv;
+        sn[i] = sv;
     }
     __syncthreads();
-    const bool first_half = j < LPH / 2;
-    const int i0 = 8 * (first_half ? j : j - LPH / 2);  // rotation index of element 0
-    for (bool first = true; base < total; base += kFastWarps * HPW, first = false) {  // warp-uniform
-        const int hh = base + sub;
-        const bool live = hh < total;
-        const bool is_q = hh < n_q, is_k = !is_q && hh < n_q + n_k, is_v = hh >= n_q + n_k;
-        if (!first) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = 0.f;
-            if (live) load8<T>(src_row + (int64_t)hh * D + 8 * j, x);
+    for (;;) {  // warp-uniform passes over the row's heads
+        h.rotate(cs, sn, i0, first_half, is_q || is_k);
+        if (live) {
+            T *dst;
+            if (is_q) {
+                dst = static_cast<T *>(a.q_out) + (int64_t)row * a.q_out_rs + (int64_t)hh * D;
+            } else {
+                const int hk = is_k ? hh - n_q : hh - n_q - n_k;
+                T *cache = static_cast<T *>(is_k ? a.k_cache : a.v_cache);
+                dst = cache + (int64_t)b * a.cache_seq + (int64_t)p * a.cache_rs + (int64_t)hk * a.cache_head;
+            }
+            store8<T>(dst + 8 * j, h.x);
         }
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
-#pragma unroll
-        for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const bool normed = !is_v || a.v_unit_norm;
-        const float r = normed ? rsqrtf(fmaf(ss, 1.f / (float)D, a.eps)) : 1.f;
-        const T *w = is_q ? static_cast<const T *>(a.q_w) : (is_k ? static_cast<const T *>(a.k_w) : nullptr);
-        float wv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-        if (live && w != nullptr) load8<T>(w + 8 * j, wv);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] *= r * wv[k];
-        float px[8];  // the rotation partner's elements
-#pragma unroll
-        for (int k = 0; k < 8; ++k) px[k] = __shfl_xor_sync(0xffffffffu, x[k], LPH / 2);
-        if (!live) continue;
-        if (!is_v) {
-            // first half: (a, b) -> a cos - b sin; second half: b -> a sin + b cos
-            const float sg = first_half ? -1.f : 1.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = fmaf(sg * px[k], sn[i0 + k], x[k] * cs[i0 + k]);
-        }
-        T *dst;
-        if (is_q) {
-            dst = static_cast<T *>(a.q_out) + ((int64_t)b * a.n_new + t) * a.q_out_rs + (int64_t)hh * D;
-        } else {
-            const int hk = is_k ? hh - n_q : hh - n_q - n_k;
-            T *cache = static_cast<T *>(is_k ? a.k_cache : a.v_cache);
-            dst = cache + (int64_t)b * a.cache_seq + (int64_t)p * a.cache_rs + (int64_t)hk * a.cache_head;
-        }
-        store8<T>(dst + 8 * j, x);
+        hh += kFastWarps * HPW;
+        if (hh - sub >= total) break;
+        live = hh < total, is_q = hh < n_q, is_k = !is_q && hh < n_q + n_k;
+        h.load(src_row, a, hh, j, live, is_q, is_k);
+        h.norm(a, is_q || is_k || a.v_unit_norm);
     }
 }
 
