@@ -22,6 +22,8 @@
 // kernel.  fp32 arithmetic throughout, one rounding to the output type.
 #include <math.h>
 
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -116,24 +118,7 @@ __global__ void __launch_bounds__(kWarps * 32) qkv_producer_kernel(const __grid_
     }
 }
 
-// 8 consecutive elements <-> registers, as 16-byte accesses
-template <typename T>
-__device__ __forceinline__ void load8(const T *p, float v[8]);
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16 *p, float v[8]) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        v[2 * k] = __uint_as_float(w[k] << 16);
-        v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    }
-}
-template <>
-__device__ __forceinline__ void load8<float>(const float *p, float v[8]) {
-    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
+// 8 consecutive elements from registers, as 16-byte stores
 template <typename T>
 __device__ __forceinline__ void store8(T *p, const float v[8]);
 template <>
@@ -147,15 +132,16 @@ __device__ __forceinline__ void store8<float>(float *p, const float v[8]) {
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// Vectorised form for head_dim 64/128/256: a head is D/8 lanes of 8 consecutive elements
-// (16-byte loads and stores), a warp holds 32/(D/8) heads at once, the sum of squares is
-// a shuffle reduction inside each head's lanes, and the rotation partner of lane j
-// (elements 8j..8j+7 of the first half) is lane j + D/16 of the same head.
+// Vectorised form for head_dim 64/128/256 and 16-byte aligned rows.  A head is D/16
+// lanes; lane j holds elements [8j, 8j+8) and their rotation partners [D/2 + 8j,
+// D/2 + 8j + 8) as two 16-byte vectors, so the rotation needs no data from other lanes
+// and the sum of squares is a shuffle reduction over the head's D/16 lanes.  A warp holds
+// 512/D heads; the CTA has just enough warps (up to 8) for one row's heads per pass.
 //
 // Only the rotation needs the position: the first pass's head rows, norm weights and the
 // position are all loaded up front, the norm of the first pass is done before the one
 // barrier that publishes the cos/sin table, and the rotation and the stores follow it.
-constexpr int kFastWarps = 8;
+constexpr int kFastMaxWarps = 8;
 
 // 8 elements held as raw 16-byte words until they are needed as floats (fewer registers)
 template <typename T>
@@ -185,59 +171,69 @@ __device__ __forceinline__ float Raw8<float>::get(int k) const {
 }
 
 template <typename T, int D>
-struct FastHead {  // one lane's 8 elements of one head, through norm and rotation
-    static constexpr int LPH = D / 8;
-    Raw8<T> xr, wr;
-    float x[8];
+struct FastHead {  // one lane's 2 x 8 elements of one head, through norm and rotation
+    static constexpr int LPH = D / 16;
+    Raw8<T> xlo, xhi, wlo, whi;
+    float lo[8], hi[8];
 
     __device__ __forceinline__ void load(const T *row, const ProducerArgs &a, int hh, int j, bool live,
                                          bool is_q, bool is_k) {
         const T *wp = is_q ? static_cast<const T *>(a.q_w) : (is_k ? static_cast<const T *>(a.k_w) : nullptr);
-        xr.fill(0u);
-        wr.fill(sizeof(T) == 2 ? 0x3f803f80u : 0x3f800000u);  // 1.0
-        if (live) xr.load(row + (int64_t)hh * D + 8 * j);
-        if (live && wp != nullptr) wr.load(wp + 8 * j);
+        const uint32_t one = sizeof(T) == 2 ? 0x3f803f80u : 0x3f800000u;  // 1.0
+        xlo.fill(0u), xhi.fill(0u), wlo.fill(one), whi.fill(one);
+        if (live) {
+            const T *h = row + (int64_t)hh * D + 8 * j;
+            xlo.load(h);
+            xhi.load(h + D / 2);
+        }
+        if (live && wp != nullptr) {
+            wlo.load(wp + 8 * j);
+            whi.load(wp + D / 2 + 8 * j);
+        }
     }
     // x <- x / sqrt(mean(x^2) + eps) * w (or x for a V head that is not normed)
     __device__ __forceinline__ void norm(const ProducerArgs &a, bool normed) {
         float ss = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            x[k] = xr.get(k);
-            ss = fmaf(x[k], x[k], ss);
+            lo[k] = xlo.get(k);
+            hi[k] = xhi.get(k);
+            ss = fmaf(lo[k], lo[k], ss);
+            ss = fmaf(hi[k], hi[k], ss);
         }
 #pragma unroll
         for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float r = normed ? rsqrtf(fmaf(ss, 1.f / (float)D, a.eps)) : 1.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] *= r * wr.get(k);
+        for (int k = 0; k < 8; ++k) {
+            lo[k] *= r * wlo.get(k);
+            hi[k] *= r * whi.get(k);
+        }
     }
-    // first half: (a, b) -> a cos - b sin; second half: b -> a sin + b cos, where the
-    // partner's elements come from lane j +- D/16 (all lanes take part in the shuffle)
-    __device__ __forceinline__ void rotate(const float *cs, const float *sn, int i0, bool first_half,
-                                           bool rotated) {
-        float px[8];
+    // (a, b) -> (a cos - b sin, a sin + b cos) for pair index i0 + k
+    __device__ __forceinline__ void rotate(const float *cs, const float *sn, int i0) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) px[k] = __shfl_xor_sync(0xffffffffu, x[k], LPH / 2);
-        if (!rotated) return;
-        const float sg = first_half ? -1.f : 1.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = fmaf(sg * px[k], sn[i0 + k], x[k] * cs[i0 + k]);
+        for (int k = 0; k < 8; ++k) {
+            const float c = cs[i0 + k], s = sn[i0 + k];
+            const float a0 = lo[k], b0 = hi[k];
+            lo[k] = fmaf(a0, c, -b0 * s);
+            hi[k] = fmaf(a0, s, b0 * c);
+        }
     }
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kFastWarps * 32, 6) qkv_producer_fast(const __grid_constant__ ProducerArgs a) {
-    constexpr int LPH = D / 8, HPW = 32 / LPH, HALF = D / 2;
+__global__ void __launch_bounds__(kFastMaxWarps * 32) qkv_producer_fast(const __grid_constant__ ProducerArgs a) {
+    constexpr int LPH = D / 16, HPW = 32 / LPH, HALF = D / 2;
     __shared__ float cs[HALF], sn[HALF];
     const int row = blockIdx.x;
     const int b = row / a.n_new, t = row - b * a.n_new;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
     const int sub = lane / LPH, j = lane % LPH;
     const T *src_row = static_cast<const T *>(a.qkv) + (int64_t)row * a.qkv_rs;
     const int n_q = a.n_heads, n_k = a.n_kv_heads, total = n_q + 2 * n_k;
-    const bool first_half = j < LPH / 2;
-    const int i0 = 8 * (first_half ? j : j - LPH / 2);  // rotation index of element 0
+    const int i0 = 8 * j;  // pair index of the lane's first element
 
     FastHead<T, D> h;
     int hh = warp * HPW + sub;
@@ -261,8 +257,8 @@ __global__ void __launch_bounds__(kFastWarps * 32, 6) qkv_producer_fast(const __
     }
     __syncthreads();
     for (;;) {  // warp-uniform passes over the row's heads
-        h.rotate(cs, sn, i0, first_half, is_q || is_k);
         if (live) {
+            if (is_q || is_k) h.rotate(cs, sn, i0);
             T *dst;
             if (is_q) {
                 dst = static_cast<T *>(a.q_out) + (int64_t)row * a.q_out_rs + (int64_t)hh * D;
@@ -271,9 +267,10 @@ __global__ void __launch_bounds__(kFastWarps * 32, 6) qkv_producer_fast(const __
                 T *cache = static_cast<T *>(is_k ? a.k_cache : a.v_cache);
                 dst = cache + (int64_t)b * a.cache_seq + (int64_t)p * a.cache_rs + (int64_t)hk * a.cache_head;
             }
-            store8<T>(dst + 8 * j, h.x);
+            store8<T>(dst + 8 * j, h.lo);
+            store8<T>(dst + D / 2 + 8 * j, h.hi);
         }
-        hh += kFastWarps * HPW;
+        hh += nwarps * HPW;
         if (hh - sub >= total) break;
         live = hh < total, is_q = hh < n_q, is_k = !is_q && hh < n_q + n_k;
         h.load(src_row, a, hh, j, live, is_q, is_k);
@@ -284,10 +281,13 @@ __global__ void __launch_bounds__(kFastWarps * 32, 6) qkv_producer_fast(const __
 template <typename T>
 cudaError_t launch_t(const ProducerArgs &a, unsigned blocks, bool vec, cudaStream_t s) {
     if (vec) {
+        // warps for one pass over the row's heads (512 / D heads per warp), at most 8
+        const int heads = a.n_heads + 2 * a.n_kv_heads, hpw = 512 / a.head_dim;
+        const int threads = 32 * std::min(kFastMaxWarps, (heads + hpw - 1) / hpw);
         switch (a.head_dim) {
-            case 64: qkv_producer_fast<T, 64><<<blocks, kFastWarps * 32, 0, s>>>(a); return cudaGetLastError();
-            case 128: qkv_producer_fast<T, 128><<<blocks, kFastWarps * 32, 0, s>>>(a); return cudaGetLastError();
-            case 256: qkv_producer_fast<T, 256><<<blocks, kFastWarps * 32, 0, s>>>(a); return cudaGetLastError();
+            case 64: qkv_producer_fast<T, 64><<<blocks, threads, 0, s>>>(a); return cudaGetLastError();
+            case 128: qkv_producer_fast<T, 128><<<blocks, threads, 0, s>>>(a); return cudaGetLastError();
+            case 256: qkv_producer_fast<T, 256><<<blocks, threads, 0, s>>>(a); return cudaGetLastError();
             default: break;
         }
     }
