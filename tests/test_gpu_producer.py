@@ -137,3 +137,40 @@ def test_producer_full_workload():
     _check(kc[:, :T].reshape(B, T, Hkv, D), rk, "bf16", "k rows")
     _check(vc[:, :T].reshape(B, T, Hkv, D), rv, "bf16", "v rows")
     assert torch.isnan(kc[:, T:].float()).all() and torch.isnan(vc[:, T:].float()).all()
+
+
+# (D, pos, T, base): rows far out, where fp32 can no longer hold p * freq exactly; the
+# last case crosses 2^24, where positions stop being exact in fp32 at all.  fp32 outputs,
+# so an angle error above ~1e-5 rad would show.  One sequence, one KV head: the caches
+# hold pos + T rows (up to 4.3 GB each).
+FAR = [
+    (64, 5_000_003, 5, 1e4),
+    (80, 9_999_998, 3, 1e4),       # the general kernel
+    (64, (1 << 24) - 3, 6, 1e4),   # crosses 2^24
+]
+
+
+@pytest.mark.parametrize("case", FAR, ids=lambda c: "D%d-pos%d" % (c[0], c[1]))
+def test_producer_far_positions(case):
+    D, p0, T, base = case
+    Hq, Hkv, cap = 2, 1, case[1] + case[2]
+    width = (Hq + 2 * Hkv) * D
+    qkv = W.normal((T, width), dtype="f32", device="cuda", seed=W.BASE_SEED + D, role="new")
+    kc = torch.full((1, cap, Hkv * D), float("nan"), dtype=torch.float32, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    q_out = torch.empty((T, Hq * D), dtype=torch.float32, device="cuda")
+    pos = torch.tensor([p0], dtype=torch.int32, device="cuda")
+    st = status_tensor()
+    binding.lat_qkv_norm_rope_append(binding.LAT_F32, qkv, qkv.stride(0), None, None, 1e-6, base,
+                                     False, q_out, q_out.stride(0), kc, vc, Hkv * D, D,
+                                     cap * Hkv * D, cap, pos, T, 1, Hq, Hkv, D, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rq, rk, rv = producer.qkv_norm_rope(qkv.reshape(1, T, width), [p0], n_heads=Hq,
+                                        n_kv_heads=Hkv, head_dim=D, q_w=None, k_w=None,
+                                        eps=1e-6, base=base)
+    _check(q_out.view(1, T, Hq, D), rq, "f32", "q")
+    _check(kc[:, p0:p0 + T].reshape(1, T, Hkv, D), rk, "f32", "k rows")
+    _check(vc[:, p0:p0 + T].reshape(1, T, Hkv, D), rv, "f32", "v rows")
+    del kc, vc
+    torch.cuda.empty_cache()
