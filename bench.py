@@ -430,60 +430,96 @@ def measure_extra(device, flush, stream, peaks, reps=10):
 
 
 def e2e_measure(step, steps, stream):
-    """Host buffers through the C ABI: upload the step's inputs from pinned memory, run,
-    download the outputs (and lse).  Returns (ms per step, h2d bytes, d2h bytes)."""
+    """Host buffers through the C ABI: every step uploads its inputs from pinned host
+    memory, runs, and downloads its outputs (and lse) into pinned host memory.  Steps are
+    pipelined over two buffer sets on three streams (upload, compute, download), so the
+    upload of step i+1 and the download of step i-1 overlap the kernels of step i, as a
+    serving loop over independent batches would run.  Returns (ms per step, h2d bytes,
+    d2h bytes), the time being the whole run's span divided by the steps."""
     if isinstance(step, PrefillStep):
         wl, inp = step.wl, step.inp
         if inp.packed is not None:
             parents = [inp.packed]
         else:
             parents = [inp.q.contiguous(), inp.k.contiguous(), inp.v.contiguous()]
-        outs = [step.out, step.lse]
+        out_names = ("out", "lse")
     elif isinstance(step, PrefillCachedStep):
         d = step.di
         parents = [step.q, d.k_cache, d.v_cache]
-        outs = [step.out, step.lse]
+        out_names = ("out", "lse")
     elif isinstance(step, ProducerStep):
         parents = [step.qkv]
-        outs = [step.q_out]  # the cache rows stay on the device for the attention kernels
+        out_names = ("q_out",)  # the cache rows stay on the device for the attention kernels
     else:
         d = step.di
         parents = [d.q, d.k_cache, d.v_cache, d.kv_lens]
-        outs = [step.out, step.lse]
+        out_names = ("out", "lse")
     hosts = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in parents]
     for h, p in zip(hosts, parents):
         h.copy_(p.cpu())
-    devs = [torch.empty_like(p) for p in parents]
-    host_outs = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    if isinstance(step, PrefillStep):
-        if inp.packed is not None:
-            qw, kw = wl.Hq * wl.D, wl.Hkv * wl.D
-            buf = devs[0]
-            args = (buf[:, :qw], buf[:, qw:qw + kw], buf[:, qw + kw:])
-        else:
-            args = tuple(devs)
-    else:
-        args = tuple(devs)
+    nbuf = 2
+    devs = [[torch.empty_like(p) for p in parents] for _ in range(nbuf)]
+    outs = [[torch.empty_like(getattr(step, n)) for n in out_names] for _ in range(nbuf)]
+    host_outs = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs[0]]
+                 for _ in range(nbuf)]
 
-    def one():
-        for dv, h in zip(devs, hosts):
-            dv.copy_(h, non_blocking=True)
-        step(*args)
-        for h, o in zip(host_outs, outs):
-            h.copy_(o, non_blocking=True)
+    def args_of(dv):
+        if isinstance(step, PrefillStep) and step.inp.packed is not None:
+            qw, kw = step.wl.Hq * step.wl.D, step.wl.Hkv * step.wl.D
+            buf = dv[0]
+            return (buf[:, :qw], buf[:, qw:qw + kw], buf[:, qw + kw:])
+        return tuple(dv)
 
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
-        one()
-    e.record(stream)
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+    keep = {n: getattr(step, n) for n in out_names}
+    ev = lambda: torch.cuda.Event()
+    up_done = [ev() for _ in range(nbuf)]
+    run_done = [ev() for _ in range(nbuf)]
+    down_done = [ev() for _ in range(nbuf)]
+    used = [False] * nbuf
+
+    def one(i):
+        k = i % nbuf
+        with torch.cuda.stream(s_up):
+            if used[k]:
+                s_up.wait_event(run_done[k])      # the kernels of step i-2 read devs[k]
+            for dv, h in zip(devs[k], hosts):
+                dv.copy_(h, non_blocking=True)
+            up_done[k].record(s_up)
+        stream.wait_event(up_done[k])
+        if used[k]:
+            stream.wait_event(down_done[k])       # step i-2's outputs are downloaded
+        for n, o in zip(out_names, outs[k]):
+            setattr(step, n, o)
+        step(*args_of(devs[k]))
+        run_done[k].record(stream)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(run_done[k])
+            for h, o in zip(host_outs[k], outs[k]):
+                h.copy_(o, non_blocking=True)
+            down_done[k].record(s_down)
+        used[k] = True
+
+    try:
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_up)
+        s_down.wait_stream(s_up)
+        stream.wait_stream(s_up)
+        for i in range(steps):
+            one(i)
+        s_up.wait_stream(s_down)
+        s_up.wait_stream(stream)
+        t1.record(s_up)
+        torch.cuda.synchronize()
+    finally:
+        for n, o in keep.items():
+            setattr(step, n, o)
+    ms = t0.elapsed_time(t1) / steps
     h2d = sum(h.numel() * h.element_size() for h in hosts)
-    d2h = sum(h.numel() * h.element_size() for h in host_outs)
+    d2h = sum(h.numel() * h.element_size() for h in host_outs[0])
     return ms, h2d, d2h
 
 
