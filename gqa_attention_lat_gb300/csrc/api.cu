@@ -162,7 +162,8 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
         kv.v_head % 8 || kv.v_seq % 8)
         return LAT_ERR_INVALID_ARG;
     lat::PrefillTcArgs a{};
-    const int bn = lat::prefill_tc_block_n(head_dim);
+    a.wide = lat::prefill_tc_wide(head_dim, seq_len, kv_len, causal, window) ? 1 : 0;
+    const int bn = lat::prefill_tc_block_n(head_dim, a.wide != 0);
     // K/V maps span exactly kv_len rows per sequence: rows past it read as zeros, so cache
     // slots beyond the visible keys (which may hold anything) never reach the MMA
     if (!make_head_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, 128) ||

@@ -113,8 +113,11 @@ struct PrefillTcArgs {
     int32_t *status;
     uint64_t timeout_ns;
     int test_skip_kv_load;         // test hook: never load KV tile 0 (forces a timeout)
+    int wide;                      // head_dim 64: the 96-key-tile form (prefill_tc_wide)
 };
-int prefill_tc_block_n(int head_dim);        // keys per KV tile for this head_dim
+// the 96-key-tile form of head_dim 64 for long key ranges (a query tile visiting ~1K keys)
+bool prefill_tc_wide(int head_dim, int seq_len, int kv_len, int causal, int window);
+int prefill_tc_block_n(int head_dim, bool wide);  // keys per KV tile
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace lat

@@ -56,14 +56,16 @@ constexpr int kChunkCols = 64;       // head-dim columns per swizzled chunk (128
 constexpr uint32_t kTmemO = 0;       // O accumulator columns [0, kOCols)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+template <int D, bool W = false>
 struct TcCfg {
     static constexpr int kQkChunks = (D + kChunkCols - 1) / kChunkCols;   // Q/K chunks
     static constexpr int kKSteps = (D + 15) / 16;                          // S MMA k-steps
     // keys per tile; head_dim 64 takes 64-key tiles so that two CTAs fit one SM (256 tensor
     // memory columns and under 113 KB of shared memory each): at that size a CTA's serial
     // chain of S MMA, softmax and P.V leaves the SM idle, and a second CTA fills the gaps
-    static constexpr int kBN = D == 64 ? 64 : (D <= 256 ? 128 : 64);
+    // W (head_dim 64 with long key ranges): 96-key tiles, which halve the per-tile fixed
+    // costs where a query tile visits a thousand keys or more, still two CTAs per SM
+    static constexpr int kBN = D == 64 ? (W ? 96 : 64) : (D <= 256 ? 128 : 64);
     static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
     static constexpr uint32_t kTmemS = D == 64 ? 64 : 256;     // S buffers at kTmemS (+ BN)
     static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
@@ -73,8 +75,8 @@ struct TcCfg {
     static constexpr int kChunkBytes = kBN * 128;                          // one [BN x 64] chunk
     static constexpr int kKTileBytes = kQkChunks * kChunkBytes;
     static constexpr int kVTileBytes = kVChunks * kChunkBytes;
-    static constexpr int kKStages = D == 64 ? 4 : (D <= 128 ? 3 : 1);
-    static constexpr int kVStages = D == 64 ? 4 : (D <= 128 ? 2 : 1);
+    static constexpr int kKStages = D == 64 ? (W ? 3 : 4) : (D <= 128 ? 3 : 1);
+    static constexpr int kVStages = D == 64 ? (W ? 3 : 4) : (D <= 128 ? 2 : 1);
     static constexpr int kQBytes = kQkChunks * kBM * 128;
     static constexpr int kQStages = D <= 128 ? 2 : 1;   // the next item's Q loads early
     static constexpr int kBarBytes = 256 + 4 * kBM * 4;  // barriers + row exchange
@@ -153,9 +155,9 @@ struct Item {
 
 // Items are numbered heaviest first (latest query tiles, which see the most keys under a
 // causal mask), then by sequence and head.
-template <int D>
+template <int D, bool W>
 __device__ __forceinline__ Item item_at(const PrefillTcArgs &a, int idx) {
-    using C = TcCfg<D>;
+    using C = TcCfg<D, W>;
     const int per_tile = a.batch * a.n_heads * C::kSplitO;
     const int n_mtiles = (a.seq_len + kBM - 1) / kBM;
     const int z = idx / per_tile, rem = idx % per_tile;
@@ -180,10 +182,10 @@ __device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
     return idx < n_items ? idx : -1;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, TcCfg<D>::kCtasPerSm)
+template <int D, bool W>
+__global__ void __launch_bounds__(kThreads, TcCfg<D, W>::kCtasPerSm)
 prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
-    using C = TcCfg<D>;
+    using C = TcCfg<D, W>;
     constexpr int BN = C::kBN;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -269,7 +271,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             for (int k = 0; ok; ++k) {
                 const int idx = item_index(k, cta, G, n_items);
                 if (idx < 0) break;
-                const Item it = item_at<D>(a, idx);
+                const Item it = item_at<D, W>(a, idx);
                 if (is_k) {
                     const int qs = qi % C::kQStages;
                     if (!mbar_wait_bounded(&q_empty[qs], ((qi / C::kQStages) & 1) ^ 1, abort_flag,
@@ -333,7 +335,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             for (int k = 0, qi = 0; ok; ++k, ++qi) {
                 const int idx = item_index(k, cta, G, n_items);
                 if (idx < 0) break;
-                const Item it = item_at<D>(a, idx);
+                const Item it = item_at<D, W>(a, idx);
                 const int n_tiles = it.band.t_end - it.band.t_begin;
                 const int qs = qi % C::kQStages;
                 if (!mbar_wait_bounded(&q_full[qs], (qi / C::kQStages) & 1, abort_flag, deadline)) {
@@ -441,7 +443,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         for (int k = 0; ok; ++k) {
             const int idx = item_index(k, cta, G, n_items);
             if (idx < 0) break;
-            const Item it = item_at<D>(a, idx);
+            const Item it = item_at<D, W>(a, idx);
             const int n_tiles = it.band.t_end - it.band.t_begin;
             const int i = it.m0 + row;                       // query row within the sequence
             const int p = i + (a.kv_len - a.seq_len);        // its absolute position
@@ -602,23 +604,31 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     }
 }
 
-template <int D>
+template <int D, bool W = false>
 cudaError_t launch_d(const PrefillTcArgs &a, int num_sms, cudaStream_t s) {
-    using C = TcCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+    using C = TcCfg<D, W>;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t n_items = (int64_t)a.batch * a.n_heads * C::kSplitO * ((a.seq_len + kBM - 1) / kBM);
     const int grid = (int)std::min<int64_t>(n_items, std::max(1, num_sms) * C::kCtasPerSm);
-    prefill_tc_kernel<D><<<grid, kThreads, C::kSmem, s>>>(a);
+    prefill_tc_kernel<D, W><<<grid, kThreads, C::kSmem, s>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int prefill_tc_block_n(int head_dim) {
+bool prefill_tc_wide(int head_dim, int seq_len, int kv_len, int causal, int window) {
+    if (head_dim != 64) return false;
+    // mean keys a query tile visits (bottom-right causal alignment, window cap)
+    double keys = causal ? (kv_len - seq_len) + seq_len / 2.0 + kBM / 2.0 : (double)kv_len;
+    if (window > 0) keys = std::min(keys, (double)window + kBM);
+    return keys >= 1024.0;
+}
+
+int prefill_tc_block_n(int head_dim, bool wide) {
     switch (head_dim) {
-        case 64: return TcCfg<64>::kBN;
+        case 64: return wide ? TcCfg<64, true>::kBN : TcCfg<64>::kBN;
         case 80: return TcCfg<80>::kBN;
         case 128: return TcCfg<128>::kBN;
         case 256: return TcCfg<256>::kBN;
@@ -630,7 +640,7 @@ int prefill_tc_block_n(int head_dim) {
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t s) {
     if (a.seq_len == 0 || a.batch == 0) return cudaSuccess;
     switch (a.head_dim) {
-        case 64: return launch_d<64>(a, num_sms, s);
+        case 64: return a.wide ? launch_d<64, true>(a, num_sms, s) : launch_d<64>(a, num_sms, s);
         case 80: return launch_d<80>(a, num_sms, s);
         case 128: return launch_d<128>(a, num_sms, s);
         case 256: return launch_d<256>(a, num_sms, s);

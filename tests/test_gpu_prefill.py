@@ -40,6 +40,11 @@ SWEEP = [
     (1, 64, 1000, 8, 2, 64, True, 300, False, "bf16"),
     (1, 130, 600, 4, 1, 512, True, 0, False, "bf16"),
     (1, 1000, 1000, 4, 2, 64, True, 0, True, "bf16"),
+    # head_dim 64 with long key ranges (a query tile visits ~1K keys or more): 96-key tiles
+    (1, 2500, 2500, 8, 2, 64, True, 0, False, "bf16"),
+    (2, 130, 1100, 4, 4, 64, False, 0, False, "bf16"),
+    (1, 3000, 3000, 4, 2, 64, True, 1100, True, "bf16"),
+    (2, 300, 2048, 4, 1, 64, True, 0, False, "bf16"),
     # fp32 (exact CUDA-core path)
     (1, 64, 64, 4, 2, 64, True, 0, False, "f32"),
     (2, 100, 100, 6, 2, 80, True, 7, False, "f32"),

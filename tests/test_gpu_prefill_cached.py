@@ -43,6 +43,7 @@ CASES = [
     (1, 4, 4, 80, 260, 200, 1, True, 0, "bf16", True),         # one new row
     (1, 16, 2, 512, 1100, 1000, 256, True, 0, "bf16", False),  # head_dim 512 (split O)
     (2, 8, 4, 128, 512, 384, 130, False, 0, "bf16", False),    # no mask: the chunk sees all
+    (2, 8, 2, 64, 2100, 2048, 300, True, 0, "bf16", False),   # 96-key tiles (long range)
     (2, 4, 2, 64, 100, 90, 30, True, 0, "f32", False),
     (1, 4, 2, 64, 96, 70, 70, True, 16, "f32", True),
 ]
