@@ -200,3 +200,21 @@ def test_tiny_f32_prefill_append_decode():
     ref, ref_lse = oracle_prefill(inp, causal=True, window=0, scale=wl.scale)
     compare(pout, ref, "f32", "tiny prefill", plse, ref_lse)
     compare(dout.view(1, 4, 64), ref[:, -1], "f32", "tiny decode", dlse, ref_lse[:, -1])
+
+
+def test_decode_large_batch_with_empty_sequences():
+    """600 sequences (more units than CTAs), lengths drawn in [0, 300] with zeros forced in:
+    empty sequences give out = 0 and lse = -inf, the rest match the oracle."""
+    B, Hq, Hkv, D, cap = 600, 8, 2, 128, 300
+    g = torch.Generator().manual_seed(W.BASE_SEED + 600)
+    lens = torch.randint(0, cap + 1, (B,), generator=g)
+    lens[::97] = 0
+    lens[1::89] = cap
+    di = W.decode_inputs(B, Hq, Hkv, D, cap, kv_lens=lens.tolist(), dtype="bf16", device="cuda",
+                         seed=W.BASE_SEED + 601)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = run_decode(di, window=0, scale=scale)
+    ref, ref_lse = oracle_decode(di, window=0, scale=scale)
+    compare(out, ref, "bf16", "B600 with empty sequences", lse, ref_lse)
+    empty = (lens == 0).nonzero().flatten().tolist()
+    assert empty and torch.all(out[empty].float() == 0)

@@ -119,3 +119,31 @@ def test_gemma4_prefill_sampled_rows(name):
     got = out.reshape(wl.B * wl.S, wl.Hq, wl.D)[idx]
     got_lse = lse.reshape(wl.B * wl.S, wl.Hq)[idx]
     compare(got, ref, "bf16", name, got_lse, ref_lse)
+
+
+# Size extremes: a 32K-row causal prefill (rows sampled), and many short sequences (more
+# items than the grid has CTAs several times over, every row compared).
+@pytest.mark.parametrize("case", [
+    (1, 32768, 4, 1, 128, 0),
+    (1, 20000, 8, 2, 64, 0),      # head_dim 64 in its 96-key-tile form
+    (1, 16384, 4, 2, 256, 4096),
+], ids=lambda c: "S%dH%d-%dD%dw%d" % (c[1], c[2], c[3], c[4], c[5]))
+def test_prefill_long_sequence_sampled_rows(case):
+    B, S, Hq, Hkv, D, window = case
+    inp = W.prefill_inputs(B, S, S, Hq, Hkv, D, dtype="bf16", device="cuda",
+                           seed=W.BASE_SEED + S + D)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = run_prefill(inp, causal=True, window=window, scale=scale)
+    rows = W.sample_rows(B * S, S, extra=[127, 128, 4095, 4096, S // 2], n_random=64)
+    ref, ref_lse = oracle_prefill(inp, causal=True, window=window, scale=scale, rows=rows)
+    idx = torch.tensor(rows, device="cuda")
+    compare(out.reshape(B * S, Hq, D)[idx], ref, "bf16", str(case),
+            lse.reshape(B * S, Hq)[idx], ref_lse)
+
+
+def test_prefill_many_short_sequences():
+    B, S, Hq, Hkv, D = 300, 37, 8, 2, 64
+    inp = W.prefill_inputs(B, S, S, Hq, Hkv, D, dtype="bf16", device="cuda", seed=W.BASE_SEED + 3)
+    out, lse = run_prefill(inp, causal=True, window=0, scale=0.125)
+    ref, ref_lse = oracle_prefill(inp, causal=True, window=0, scale=0.125)
+    compare(out, ref, "bf16", "300 x 37 rows", lse, ref_lse)
