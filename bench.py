@@ -7,15 +7,17 @@ A step is one pass of the attention hot path over one batch of synthetic input. 
 headline workload is the Qwen3-0.6B-shaped bf16 prefill (batch 8, 512 tokens, 16 query
 heads, 8 KV heads, head_dim 64, causal) read with row strides from one packed
 [4096, 2048] QKV buffer.  Each timed step is bracketed by CUDA events on the launching
-stream, with a 256 MiB write between steps so every step starts with a cold L2.
+stream; before every step a 256 MiB write and a 256 MiB read leave L2 cold and clean.
 
 `value` is TFLOP/s of algorithmic work (4*D FLOPs per visible query-key pair per head).
-`e2e` repeats the step through the C ABI from pinned host buffers, with the QKV upload
-and the output/lse download inside the timed region.  `roofline` rates the prefill kernel
-against the HBM roofline (this workload's arithmetic intensity is below the ridge point).
-`workloads` adds the other named shapes (Gemma-4 sliding/global prefill, both decode
-shapes), each rated against its own roofline.  `cpu_baseline` is the fp64 oracle timed on
-the host cores.  With --impl reference the oracle itself is the timed arm.
+`e2e` runs the steps through the C ABI from pinned host buffers: every step uploads its
+inputs and downloads its output and lse, pipelined over two buffer sets on three streams.
+`roofline` rates the prefill kernel against the HBM roofline (this workload's arithmetic
+intensity is below the ridge point).  `workloads` adds the other named shapes (Gemma-4
+sliding/global and Gemma-2 softcap prefill, chunked prefill on a cache, the three decode
+shapes, the attention-input producer), each rated against its own roofline.
+`cpu_baseline` is the fp64 oracle timed on the host cores.  With --impl reference the
+oracle itself is the timed arm.  --workload NAME makes any named workload the timed one.
 
 Multi-GPU runs (torchrun) are independent replicas of the same workload (the path has no
 exchange step); every rank times its own steps and the slowest rank sets the time.
