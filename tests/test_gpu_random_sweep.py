@@ -2,14 +2,15 @@
 
 The hand-picked sweeps cover the named configurations and their edges; this one draws
 batch, lengths, head counts (GQA group 1..8), head_dim, mask, window, dtype and layout at
-random from a fixed seed, so every run checks the same 48 cases and a failure is
-reproducible from its id."""
+random from a fixed seed, so every run checks the same 64 cases (the next rows' entry
+points included) and a failure is reproducible from its id."""
 import math
 import random
 
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from gpu_helpers import compare, ensure_library, oracle_decode, oracle_prefill, run_decode, \
     run_prefill
@@ -87,4 +88,96 @@ def test_random_decode(case):
     scale = 1.0 / math.sqrt(D)
     out, lse = run_decode(di, window=window, scale=scale)
     ref, ref_lse = oracle_decode(di, window=window, scale=scale)
+    compare(out, ref, dtype, str(case), lse, ref_lse)
+
+
+def _next_row_cases(n=16, seed=20262):
+    """Random cases for the next rows' entry points: chunked prefill from a cache, score
+    softcap (prefill and decode) and ring-cache decode."""
+    rng = random.Random(seed)
+    cases = []
+    for k in range(n):
+        kind = ("cached", "softcap_prefill", "softcap_decode", "ring")[k % 4]
+        D = rng.choice([64, 128, 256] if kind != "cached" else HEAD_DIMS)
+        G = rng.choice([1, 2, 4, 8])
+        Hkv = rng.choice([1, 2])
+        dtype = "f32" if rng.random() < 0.2 else "bf16"
+        B = rng.randint(1, 4)
+        if kind == "cached":
+            L = rng.randint(1, 900)
+            S = rng.randint(1, L)
+            cap = L + rng.randint(0, 300)
+            cases.append((kind, B, Hkv * G, Hkv, D, dtype, dict(L=L, S=S, cap=cap,
+                                                                  head_major=rng.random() < 0.5,
+                                                                  window=rng.choice([0, rng.randint(1, 500)]))))
+        elif kind == "softcap_prefill":
+            S = rng.randint(1, 300)
+            cases.append((kind, B, Hkv * G, Hkv, D, dtype, dict(S=S, L=S + rng.choice([0, 100]),
+                                                                  cap=rng.uniform(0.5, 5.0))))
+        elif kind == "softcap_decode":
+            cap = rng.randint(1, 1500)
+            cases.append((kind, B, Hkv * G, Hkv, D, dtype,
+                          dict(kvcap=cap, lens=[rng.randint(0, cap) for _ in range(B)],
+                               cap=rng.uniform(0.5, 5.0))))
+        else:
+            C = rng.randint(16, 700)
+            cases.append((kind, B, Hkv * G, Hkv, D, dtype,
+                          dict(C=C, W=rng.randint(1, C),
+                               lens=[rng.randint(1, 4 * C) for _ in range(B)])))
+    return cases
+
+
+@pytest.mark.parametrize("case", _next_row_cases(), ids=lambda c: "%s-B%dH%d-%dD%d-%s" % c[:6])
+def test_random_next_rows(case):
+    kind, B, Hq, Hkv, D, dtype, p = case
+    scale = 1.0 / math.sqrt(D)
+    seed = W.BASE_SEED + 11 * D + B + Hq
+    if kind == "cached":
+        from test_gpu_prefill_cached import run_cached
+        L, S, cap, window = p["L"], p["S"], p["cap"], p["window"]
+        di = W.decode_inputs(B, Hq, Hkv, D, cap, kv_lens=L, dtype=dtype, device="cuda", seed=seed)
+        q = W.normal((B * S, Hq * D), dtype=dtype, device="cuda", seed=seed, role="chunk_q")
+        kt, vt = di.cache_heads("k_cache"), di.cache_heads("v_cache")
+        if p["head_major"]:
+            kc, vc = kt.permute(0, 2, 1, 3).contiguous(), vt.permute(0, 2, 1, 3).contiguous()
+            strides = (D, cap * D, Hkv * cap * D)
+        else:
+            kc, vc, strides = di.k_cache, di.v_cache, (Hkv * D, D, cap * Hkv * D)
+        out, lse = run_cached(q, kc, vc, *strides, B, S, L, Hq, Hkv, D, True, window, scale, dtype)
+        ref, ref_lse = oracle.prefill(q.view(B, S, Hq, D), kt[:, :L], vt[:, :L], causal=True,
+                                      window=window, scale=scale)
+    elif kind == "softcap_prefill":
+        from test_gpu_softcap import run_prefill_softcap
+        inp = W.prefill_inputs(B, p["S"], p["L"], Hq, Hkv, D, dtype=dtype, device="cuda", seed=seed)
+        out, lse = run_prefill_softcap(inp, True, 0, 2 * scale, p["cap"])
+        ref, ref_lse = oracle.prefill(inp.heads("q"), inp.heads("k"), inp.heads("v"), causal=True,
+                                      window=0, scale=2 * scale, softcap=p["cap"])
+    elif kind == "softcap_decode":
+        from gpu_helpers import DT, DecodeRun, status_tensor
+        from gqa_attention_lat_gb300 import binding
+        kvcap = p["kvcap"]
+        di = W.decode_inputs(B, Hq, Hkv, D, kvcap, kv_lens=p["lens"], dtype=dtype, device="cuda",
+                             seed=seed)
+        run = DecodeRun(dtype, B, Hq, Hkv, D, kvcap)
+        out = torch.full((B, Hq * D), float("nan"), dtype=di.q.dtype, device="cuda")
+        lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+        st = status_tensor()
+        binding.lat_attn_decode_softcap(DT[dtype], di.q, di.q.stride(0), di.k_cache, di.v_cache,
+                                        Hkv * D, D, kvcap * Hkv * D, di.kv_lens, kvcap, out,
+                                        out.stride(0), lse, B, Hq, Hkv, D, 0, 2 * scale, p["cap"],
+                                        run.ws, run.nbytes, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        out = out.view(B, Hq, D)
+        ref, ref_lse = oracle.decode(di.q_heads(), di.cache_heads("k_cache"),
+                                     di.cache_heads("v_cache"), p["lens"], window=0,
+                                     scale=2 * scale, softcap=p["cap"])
+    else:
+        from test_gpu_ring import make_ring, run_ring
+        C, Wn, lens = p["C"], p["W"], p["lens"]
+        kr, vr, kh, vh = make_ring(B, Hkv, D, C, Wn, lens, dtype, seed)
+        q = W.normal((B, Hq * D), dtype=dtype, device="cuda", seed=seed, role="q")
+        lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        out, lse = run_ring(q, kr, vr, C, lens_t, max(lens), B, Hq, Hkv, D, Wn, scale, dtype)
+        ref, ref_lse = oracle.decode(q.view(B, Hq, D), kh, vh, lens, window=Wn, scale=scale)
     compare(out, ref, dtype, str(case), lse, ref_lse)
