@@ -1,0 +1,49 @@
+"""bench.py's JSON line (the reference arm runs the oracle, so it needs no GPU): one line
+with the contract's keys, and the ours-arm helpers that build the line."""
+import json
+import os
+import subprocess
+import sys
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+             "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"}
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "1"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert BASE_KEYS <= set(d)
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["steps"] == 1
+    assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"].startswith(bench.HEADLINE)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_every_workload_has_a_config_description():
+    for name, wl in W.WORKLOADS.items():
+        c = bench.workload_config(wl)
+        assert c["workload"].startswith(name) and c["l2"] and c["parallelism"] == "replicas"
+
+
+def test_algorithmic_work_of_the_headline():
+    """4 D Hq B flops per visible pair; Q + K + V read once, out + lse written once."""
+    wl = W.WORKLOADS[bench.HEADLINE]
+    flops, bytes_, pairs = bench.prefill_work(wl)
+    assert pairs == 512 * 513 // 2
+    assert flops == 4 * 64 * 16 * 8 * pairs
+    assert bytes_ == 8 * 512 * (16 + 8 + 8) * 64 * 2 + 8 * 512 * 16 * 64 * 2 + 8 * 512 * 16 * 4
