@@ -47,3 +47,25 @@ def test_algorithmic_work_of_the_headline():
     assert pairs == 512 * 513 // 2
     assert flops == 4 * 64 * 16 * 8 * pairs
     assert bytes_ == 8 * 512 * (16 + 8 + 8) * 64 * 2 + 8 * 512 * 16 * 64 * 2 + 8 * 512 * 16 * 4
+
+
+import pytest  # noqa: E402
+
+
+@pytest.mark.gpu
+def test_ours_arm_prints_one_contract_line(cuda_device):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "3",
+                        "--warmup", "3", "--no-extra", "--no-cpu"], capture_output=True,
+                       text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert BASE_KEYS <= set(d) and d["n_gpus"] == 1 and d["steps"] == 3
+    assert d["value"] > 0 and d["gpu_launches"] == 3
+    rf = d["roofline"]
+    assert rf["bound"] in ("hbm", "tensor") and 0 < rf["frac"] < 2 and rf["peak"] > 0
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    e2e = d["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
