@@ -89,12 +89,23 @@ def decode_work(wl, kv_lens):
     return flops, float(bytes_), keys
 
 
+def code_lines(text):
+    """The source without // comments and blank lines: what the hash of a kernel covers,
+    so that editing a comment does not orphan its ncu summary."""
+    out = []
+    for line in text.splitlines():
+        line = line.split("//", 1)[0].rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out) + "\n"
+
+
 def kernel_source_hash(names):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gqa_attention_lat_gb300", "csrc")
     for n in names:
-        with open(os.path.join(csrc, n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, n)) as f:
+            h.update(code_lines(f.read()).encode())
     return h.hexdigest()[:16]
 
 

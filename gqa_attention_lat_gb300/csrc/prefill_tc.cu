@@ -8,7 +8,11 @@
 // Inference Path, section 7; target architecture, open question Q2).
 //
 // How (GB300 design; the pages' Metal kernels are prior art only):
-//  * One CTA owns a 128-row query tile of one head (one TMEM lane per query row).
+//  * A unit of work ("item") is a 128-row query tile of one head (one TMEM lane per query
+//    row).  The grid is persistent, one CTA per SM (two for head_dim 64), and CTA c walks
+//    the items heaviest first, dealt forwards and backwards in turn; its K/V rings, S
+//    buffers and barrier phases run on across items.  head_dim 64 uses 64-key tiles, or
+//    96-key tiles where a query tile visits about 1K keys or more (prefill_tc_wide).
 //  * Warp roles: warps 0-7 run the softmax as two warpgroups that split each S tile's
 //    columns (thread t of a warpgroup <-> query row t; the two halves meet through a
 //    small shared-memory exchange for the row max and sum), warp 8 loads Q and K tiles
