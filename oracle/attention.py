@@ -18,6 +18,8 @@ kv_append(k_cache, v_cache, k_new, v_new, pos)
     The in-place cache append of the same page (section 1, the in-place
     ``--kv-cache-kernel`` mode; section 3, "KV cache append"): rows
     ``pos[b] .. pos[b]+n_new-1`` of sequence b take the new rows.  A plain copy.
+kv_append_ring(k_cache, v_cache, k_new, v_new, pos)
+    The same copy into a ring cache of ``cap`` rows: position p goes to row p % cap.
 """
 from __future__ import annotations
 
@@ -166,4 +168,29 @@ def kv_append(k_cache, v_cache, k_new, v_new, pos):
             raise IndexError("append rows [%d, %d) outside capacity %d" % (p, p + n_new, cap))
         kc[b, p:p + n_new] = k_new[b]
         vc[b, p:p + n_new] = v_new[b]
+    return kc, vc
+
+
+def kv_append_ring(k_cache, v_cache, k_new, v_new, pos):
+    """The same copy into a ring cache that keeps only its last ``cap`` positions, as a
+    sliding-window layer does (hf2q "Current Inference Path", section 2 step 1: window
+    1024; hf2q target architecture, section 3.3: per-layer caches): position p lives in
+    row p % cap, so new row t of sequence b lands in row (pos[b] + t) % cap.
+
+    k_cache, v_cache: [B, cap, Hkv, D]; k_new, v_new: [B, n_new, Hkv, D], n_new <= cap.
+    Returns fresh arrays; raises IndexError for a negative position.
+    """
+    kc, vc = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+    k_new, v_new = np.asarray(k_new), np.asarray(v_new)
+    B, cap = kc.shape[:2]
+    n_new = k_new.shape[1]
+    if n_new > cap:
+        raise IndexError("%d new rows do not fit a ring of %d" % (n_new, cap))
+    for b in range(B):
+        p = int(pos[b])
+        if p < 0:
+            raise IndexError("negative position %d" % p)
+        for t in range(n_new):
+            kc[b, (p + t) % cap] = k_new[b, t]
+            vc[b, (p + t) % cap] = v_new[b, t]
     return kc, vc

@@ -82,6 +82,44 @@ def test_kv_append_oracle():
         oracle.kv_append(kc, vc, kn, vn, [0, 6])
 
 
+def test_kv_append_ring_without_wrap_is_the_linear_append():
+    """Rows that stay inside the ring land where the linear append puts them."""
+    r = np.random.default_rng(5)
+    kc, vc = r.standard_normal((2, 8, 2, 4)), r.standard_normal((2, 8, 2, 4))
+    kn, vn = r.standard_normal((2, 3, 2, 4)), r.standard_normal((2, 3, 2, 4))
+    lin = oracle.kv_append(kc, vc, kn, vn, [0, 5])
+    ring = oracle.kv_append_ring(kc, vc, kn, vn, [0, 5])
+    assert np.array_equal(lin[0], ring[0]) and np.array_equal(lin[1], ring[1])
+
+
+def test_kv_append_ring_keeps_the_last_positions():
+    """Appending a history chunk by chunk into a ring of C rows leaves, in row r, the
+    latest position j with j % C == r (found here by scanning the history backwards),
+    and the value rows travel with their key rows."""
+    r = np.random.default_rng(6)
+    B, C, H, D, n_total, chunk = 2, 7, 2, 3, 40, 5
+    kh = r.standard_normal((B, n_total, H, D))
+    vh = r.standard_normal((B, n_total, H, D))
+    kc = np.full((B, C, H, D), np.nan)
+    vc = np.full((B, C, H, D), np.nan)
+    for p0 in range(0, n_total, chunk):
+        kc, vc = oracle.kv_append_ring(kc, vc, kh[:, p0:p0 + chunk], vh[:, p0:p0 + chunk],
+                                       [p0, p0])
+        n = p0 + chunk
+        for row in range(C):
+            latest = next((j for j in range(n - 1, -1, -1) if j % C == row), None)
+            if latest is None:
+                assert np.isnan(kc[:, row]).all() and np.isnan(vc[:, row]).all()
+            else:
+                assert np.array_equal(kc[:, row], kh[:, latest])
+                assert np.array_equal(vc[:, row], vh[:, latest])
+    # a chunk longer than the ring, or a negative position, is refused
+    with pytest.raises(IndexError):
+        oracle.kv_append_ring(kc, vc, kh[:, :C + 1], vh[:, :C + 1], [0, 0])
+    with pytest.raises(IndexError):
+        oracle.kv_append_ring(kc, vc, kh[:, :2], vh[:, :2], [0, -1])
+
+
 # ------------------------------------------------------------------------------------
 # planted mistakes: each edit below is a plausible slip in the oracle's C source; the
 # pins must reject every one of them.
