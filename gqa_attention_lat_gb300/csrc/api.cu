@@ -161,6 +161,8 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
         out_rs % 8 || kv.k_row % 8 || kv.k_head % 8 || kv.k_seq % 8 || kv.v_row % 8 ||
         kv.v_head % 8 || kv.v_seq % 8)
         return LAT_ERR_INVALID_ARG;
+    if (lat::prefill_tc_items(batch, n_heads, head_dim, seq_len) > lat::kPrefillMaxItems)
+        return LAT_ERR_UNSUPPORTED;
     lat::PrefillTcArgs a{};
     a.wide = lat::prefill_tc_wide(head_dim, seq_len, kv_len, causal, window) ? 1 : 0;
     const int bn = lat::prefill_tc_block_n(head_dim, a.wide != 0);
@@ -339,6 +341,8 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         q_rs % 8 || cache_rs % 8 || cache_head_stride % 8 || cache_seq_stride % 8 || out_rs % 8)
         return LAT_ERR_INVALID_ARG;
+    if (lat::decode_bf16_units(batch, n_heads, n_kv_heads) >= lat::kDecodeMaxUnits)
+        return LAT_ERR_UNSUPPORTED;
     int sms = 0;
     if (!current_sm_count(&sms)) return LAT_ERR_CUDA;
     // rows per sequence: the ring, or every position up to max_kv_len; the scratch layout

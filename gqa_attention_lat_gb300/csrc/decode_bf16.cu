@@ -743,8 +743,14 @@ static int min_seg_for(int range, int T) {
     return (m + T - 1) / T * T;
 }
 
+int64_t decode_bf16_units(int batch, int n_heads, int n_kv_heads) {
+    const int G = n_heads / n_kv_heads;
+    return (int64_t)batch * n_kv_heads * ((G + kHeadsPerBlock - 1) / kHeadsPerBlock);
+}
+
 bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
                       int window, int num_sms, DecodePlan *p) {
+    if (decode_bf16_units(batch, n_heads, n_kv_heads) >= kDecodeMaxUnits) return false;
     int T, occ;
     switch (head_dim) {
         case 64: T = tile_keys<64>(); occ = ctas_per_sm<64>(); break;

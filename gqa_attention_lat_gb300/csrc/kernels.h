@@ -96,6 +96,10 @@ struct DecodePlan {
 // Chooses the split size and the scratch layout; false when the shape is not built.
 bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int max_kv_len,
                       int window, int num_sms, DecodePlan *plan);
+// work units of one decode launch (sequence x KV head x block of <= 8 query heads); the
+// split-KV merge tickets carry a unit index in 23 bits, so plans stop below kDecodeMaxUnits
+int64_t decode_bf16_units(int batch, int n_heads, int n_kv_heads);
+constexpr int64_t kDecodeMaxUnits = int64_t(1) << 23;
 int decode_bf16_tile_keys(int head_dim);     // cache rows per TMA box for this head_dim
 cudaError_t launch_decode_bf16(const DecodeArgs &a, int grid, cudaStream_t s);
 
@@ -118,6 +122,10 @@ struct PrefillTcArgs {
 // the 96-key-tile form of head_dim 64 for long key ranges (a query tile visiting ~1K keys)
 bool prefill_tc_wide(int head_dim, int seq_len, int kv_len, int causal, int window);
 int prefill_tc_block_n(int head_dim, bool wide);  // keys per KV tile
+// work items of one prefill launch (query tile x head x output-column part); the kernel
+// numbers them in int32, so the host refuses shapes above kPrefillMaxItems
+int64_t prefill_tc_items(int batch, int n_heads, int head_dim, int seq_len);
+constexpr int64_t kPrefillMaxItems = int64_t(1) << 30;
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace lat

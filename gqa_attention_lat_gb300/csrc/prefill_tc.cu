@@ -641,8 +641,15 @@ int prefill_tc_block_n(int head_dim, bool wide) {
     }
 }
 
+int64_t prefill_tc_items(int batch, int n_heads, int head_dim, int seq_len) {
+    const int split = head_dim == 512 ? TcCfg<512>::kSplitO : 1;
+    return (int64_t)batch * n_heads * split * ((seq_len + kBM - 1) / kBM);
+}
+
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t s) {
     if (a.seq_len == 0 || a.batch == 0) return cudaSuccess;
+    if (prefill_tc_items(a.batch, a.n_heads, a.head_dim, a.seq_len) > kPrefillMaxItems)
+        return cudaErrorInvalidValue;
     switch (a.head_dim) {
         case 64: return a.wide ? launch_d<64, true>(a, num_sms, s) : launch_d<64>(a, num_sms, s);
         case 80: return launch_d<80>(a, num_sms, s);

@@ -59,7 +59,7 @@ typedef enum { LAT_F32 = 0, LAT_BF16 = 1 } lat_dtype;
 typedef enum {
     LAT_OK = 0,
     LAT_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride, bad ratio   */
-    LAT_ERR_UNSUPPORTED = 2, /* head_dim or dtype combination not built              */
+    LAT_ERR_UNSUPPORTED = 2, /* head_dim or dtype not built, or a size past a limit  */
     LAT_ERR_WORKSPACE = 3,   /* decode workspace missing or too small                */
     LAT_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, attribute) */
     LAT_ERR_BOUNDS = 5,      /* device: a cache position or kv_len out of range       */
@@ -84,6 +84,9 @@ const char *lat_status_string(lat_status s);
  * For LAT_BF16, q, k, v and out must be 16-byte aligned and q_rs, k_rs, v_rs, out_rs
  * multiples of 8 (the tensor-memory-access unit reads 16-byte aligned rows and the
  * epilogue writes 16-byte vectors), else LAT_ERR_INVALID_ARG.
+ * Size limits (LAT_ERR_UNSUPPORTED): batch <= 65535, ceil(seq_len / 128) <= 65535, and
+ * for LAT_BF16 at most 2^30 work items, an item being one 128-row query tile of one
+ * query head (two items per tile and head at head_dim 512).
  * `out` must not overlap q, k or v.
  */
 lat_status lat_attn_prefill(lat_dtype dt, const void *q, int64_t q_rs, const void *k,
@@ -175,6 +178,9 @@ size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int 
  * out_rs, cache_rs, cache_head_stride, cache_seq_stride multiples of 8 (tiles arrive
  * through the tensor-memory-access unit and results leave in 16-byte vectors), else
  * LAT_ERR_INVALID_ARG.
+ * Size limits (LAT_ERR_UNSUPPORTED): batch <= 65535 and, for LAT_BF16, fewer than 2^23
+ * work units, a unit being one sequence, one KV head and a block of up to 8 of its
+ * query heads (batch * n_kv_heads * ceil(n_heads / n_kv_heads / 8)).
  */
 lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
                            const void *v_cache, int64_t cache_rs, int64_t cache_head_stride,

@@ -49,6 +49,19 @@ def compare(got, ref, dtype, what, lse_got=None, lse_ref=None):
     return float(err.max()), float(err.mean())
 
 
+def assert_bits_equal(got, ref, what):
+    """Byte work (cache appends) is exact: every element equal to the expected value and
+    NaN exactly where the expected array holds NaN.  `got` is a torch tensor whose
+    values convert to float64 exactly (bf16 or fp32), `ref` a float array."""
+    g = got.detach().float().cpu().numpy().astype(np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, "%s: shape %s vs %s" % (what, g.shape, r.shape)
+    assert np.array_equal(np.isnan(g), np.isnan(r)), "%s: NaN pattern differs" % what
+    fin = ~np.isnan(r)
+    bad = np.count_nonzero(g[fin] != r[fin])
+    assert bad == 0, "%s: %d elements differ" % (what, bad)
+
+
 def run_prefill(inp, *, causal, window, scale, out_pad=0, with_lse=True, stream=None):
     """Run lat_attn_prefill on PrefillInputs; returns (out [B,S,Hq,D], lse [B,S,Hq])."""
     dev = inp.q.device

@@ -7,10 +7,18 @@ import re
 
 import pytest
 
+import torch
+
 from gqa_attention_lat_gb300 import binding
 from gqa_attention_lat_gb300.build import INCLUDE, build_library
 
 LAT_F32, LAT_BF16 = binding.LAT_F32, binding.LAT_BF16
+
+# These checks hand the library addresses that are never valid device memory and rely on
+# the host rejecting the call before any launch.  They run only where no GPU is visible,
+# so that a change in the order of the checks can never launch on them.
+no_device = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake-pointer host checks run only without a GPU")
 
 
 @pytest.fixture(scope="module")
@@ -73,13 +81,23 @@ def _prefill(**kw):
     (dict(q_rs=512), binding.LAT_ERR_INVALID_ARG),                    # row narrower than heads
     (dict(dt=7), binding.LAT_ERR_INVALID_ARG),
     (dict(scale=float("nan")), binding.LAT_ERR_INVALID_ARG),
+    (dict(batch=65536), binding.LAT_ERR_UNSUPPORTED),
+    # 65535 sequences x 32768 heads x 1 query tile = 2^31 - 2^15 items: past the 2^30 the
+    # kernel numbers in int32 (each factor alone is within its own limit)
+    (dict(batch=65535, n_heads=32768, n_kv_heads=32768, q_rs=32768 * 64, k_rs=32768 * 64,
+          v_rs=32768 * 64, out_rs=32768 * 64), binding.LAT_ERR_UNSUPPORTED),
+    # head_dim 512 has two items per query tile and head: 65535 x 16384 x 2 > 2^30
+    (dict(batch=65535, n_heads=16384, n_kv_heads=16384, head_dim=512, q_rs=16384 * 512,
+          k_rs=16384 * 512, v_rs=16384 * 512, out_rs=16384 * 512), binding.LAT_ERR_UNSUPPORTED),
 ])
+@no_device
 def test_prefill_rejects_on_host(lib, kw, code):
     with pytest.raises(binding.LatError) as e:
         _prefill(**kw)
     assert e.value.status == code
 
 
+@no_device
 def test_prefill_empty_is_a_no_op(lib):
     _prefill(batch=0)
     _prefill(seq_len=0, kv_len=0)
@@ -105,13 +123,20 @@ def _decode(**kw):
     (dict(k_cache=FAKE + 4), binding.LAT_ERR_INVALID_ARG),
     (dict(out=FAKE + 8), binding.LAT_ERR_INVALID_ARG),                # bf16 output misaligned
     (dict(out_rs=4100), binding.LAT_ERR_INVALID_ARG),                 # not a multiple of 8
+    (dict(batch=65536), binding.LAT_ERR_UNSUPPORTED),
+    # 65535 sequences x 129 KV heads (one head block each) = 8.45M units >= 2^23, the
+    # unit field of the split-KV merge tickets
+    (dict(batch=65535, n_heads=129, n_kv_heads=129, q_rs=129 * 128, out_rs=129 * 128,
+          cache_rs=129 * 128, cache_seq_stride=4096 * 129 * 128), binding.LAT_ERR_UNSUPPORTED),
 ])
+@no_device
 def test_decode_rejects_on_host(lib, kw, code):
     with pytest.raises(binding.LatError) as e:
         _decode(**kw)
     assert e.value.status == code
 
 
+@no_device
 def test_decode_empty_batch_is_a_no_op(lib):
     _decode(batch=0)
 
@@ -123,6 +148,7 @@ def test_workspace_size_rejects_bad_shapes(lib):
 
 
 @pytest.mark.parametrize("cap", [-1.0, float("inf"), float("nan")])
+@no_device
 def test_softcap_must_be_finite_and_non_negative(lib, cap):
     with pytest.raises(binding.LatError) as e:
         binding.lat_attn_prefill_softcap(LAT_BF16, FAKE, 1024, FAKE, 512, FAKE, 512, FAKE, 1024,
@@ -140,6 +166,7 @@ def test_softcap_must_be_finite_and_non_negative(lib, cap):
     (300, 256, binding.LAT_ERR_INVALID_ARG),    # the window must fit in the ring
     (100, 0, binding.LAT_ERR_INVALID_ARG),      # no ring
 ])
+@no_device
 def test_ring_decode_rejects_on_host(lib, window, ring, code):
     with pytest.raises(binding.LatError) as e:
         binding.lat_attn_decode_ring(LAT_BF16, FAKE, 4096, FAKE, FAKE, 1024, 128, 256 * 1024,
@@ -148,6 +175,7 @@ def test_ring_decode_rejects_on_host(lib, window, ring, code):
     assert e.value.status == code
 
 
+@no_device
 def test_ring_append_rejects_more_rows_than_the_ring(lib):
     with pytest.raises(binding.LatError) as e:
         binding.lat_kv_append_ring(LAT_BF16, FAKE, FAKE, 1024, 128, 64 * 1024, 64, FAKE, FAKE,
@@ -174,12 +202,14 @@ def _prefill_cached(**kw):
     (dict(v_cache=FAKE + 8), binding.LAT_ERR_INVALID_ARG),            # bf16 misaligned
     (dict(scale=float("inf")), binding.LAT_ERR_INVALID_ARG),
 ])
+@no_device
 def test_prefill_cached_rejects_on_host(lib, kw, code):
     with pytest.raises(binding.LatError) as e:
         _prefill_cached(**kw)
     assert e.value.status == code
 
 
+@no_device
 def test_prefill_cached_empty_is_a_no_op(lib):
     _prefill_cached(seq_len=0)
     _prefill_cached(batch=0)
@@ -200,12 +230,14 @@ def _append(**kw):
     (dict(pos=None), binding.LAT_ERR_INVALID_ARG),
     (dict(new_rs=512), binding.LAT_ERR_INVALID_ARG),
 ])
+@no_device
 def test_append_rejects_on_host(lib, kw, code):
     with pytest.raises(binding.LatError) as e:
         _append(**kw)
     assert e.value.status == code
 
 
+@no_device
 def test_append_nothing_is_a_no_op(lib):
     _append(n_new=0)
     _append(batch=0)
@@ -236,12 +268,14 @@ def _producer(**kw):
     (dict(cache_rs=0), binding.LAT_ERR_INVALID_ARG),
     (dict(batch=-1), binding.LAT_ERR_INVALID_ARG),
 ])
+@no_device
 def test_producer_rejects_on_host(lib, kw, code):
     with pytest.raises(binding.LatError) as e:
         _producer(**kw)
     assert e.value.status == code
 
 
+@no_device
 def test_producer_nothing_is_a_no_op(lib):
     _producer(n_new=0)
     _producer(batch=0)

@@ -7,8 +7,8 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import (DT, DecodeRun, compare, ensure_library, oracle_decode, oracle_prefill,
-                         run_decode, run_prefill, status_tensor)
+from gpu_helpers import (DT, DecodeRun, assert_bits_equal, compare, ensure_library,
+                         oracle_decode, oracle_prefill, run_decode, run_prefill, status_tensor)
 from gqa_attention_lat_gb300 import binding
 
 pytestmark = pytest.mark.gpu
@@ -154,21 +154,25 @@ def test_append_then_decode(dtype):
     v_new = packed[:, (Hq + Hkv) * D:]
     pos = torch.tensor([100, 7, 253], dtype=torch.int32, device="cuda")
     before_k = di.k_cache.clone()
+    before_v = di.v_cache.clone()
     st = status_tensor()
     # the third sequence does not fit (253 + 5 > 256): skipped whole, status BOUNDS
     binding.lat_kv_append(DT[dtype], di.k_cache, di.v_cache, Hkv * D, D, cap * Hkv * D, cap,
                           k_new, v_new, packed.stride(0), pos, n_new, B, Hkv, D, st)
     torch.cuda.synchronize()
     assert st.item() == binding.LAT_ERR_BOUNDS
-    ok_k, ok_v = oracle.kv_append(
-        before_k[:2].view(2, cap, Hkv, D).cpu().float().numpy(),
-        before_k[:2].view(2, cap, Hkv, D).cpu().float().numpy(),
-        k_new.reshape(B, n_new, Hkv, D)[:2].cpu().float().numpy(),
-        k_new.reshape(B, n_new, Hkv, D)[:2].cpu().float().numpy(), [100, 7])
-    got = di.k_cache[:2].view(2, cap, Hkv, D).cpu().float().numpy()
-    assert np.array_equal(np.isnan(got), np.isnan(ok_k))
-    assert np.array_equal(np.nan_to_num(got), np.nan_to_num(ok_k))
-    assert torch.equal(di.k_cache[2].isnan(), before_k[2].isnan())  # untouched
+
+    def heads(t, rows):
+        return t.reshape(t.shape[0], rows, Hkv, D)[:2].cpu().float().numpy()
+    ok_k, ok_v = oracle.kv_append(heads(before_k, cap), heads(before_v, cap),
+                                  heads(k_new.reshape(B, n_new, Hkv * D), n_new),
+                                  heads(v_new.reshape(B, n_new, Hkv * D), n_new), [100, 7])
+    # both caches, bit for bit (the copy is exact in either dtype), NaN pattern included
+    assert_bits_equal(di.k_cache[:2].view(2, cap, Hkv, D), ok_k, "K cache")
+    assert_bits_equal(di.v_cache[:2].view(2, cap, Hkv, D), ok_v, "V cache")
+    # the sequence that did not fit is untouched in both caches
+    assert_bits_equal(di.k_cache[2], before_k[2].cpu().float().numpy(), "K cache, skipped")
+    assert_bits_equal(di.v_cache[2], before_v[2].cpu().float().numpy(), "V cache, skipped")
     # decode the two grown sequences at their new lengths
     di.kv_lens = torch.tensor([105, 12, 253], dtype=torch.int32, device="cuda")
     out, lse = run_decode(di, window=0, scale=0.1)

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import DT, DecodeRun, compare, ensure_library, status_tensor
+from gpu_helpers import DT, DecodeRun, assert_bits_equal, compare, ensure_library, status_tensor
 from gqa_attention_lat_gb300 import binding
 
 pytestmark = pytest.mark.gpu
@@ -88,6 +88,9 @@ def test_ring_append_then_decode_follows_the_history():
     q = W.normal((B, Hq * D), dtype="bf16", device="cuda", seed=5, role="q")
     kr = torch.full((B, C, Hkv * D), float("nan"), dtype=torch.bfloat16, device="cuda")
     vr = torch.full_like(kr, float("nan"))
+    # the oracle's ring, appended alongside and compared bit for bit after every append
+    ok_k = np.full((B, C, Hkv, D), np.nan)
+    ok_v = np.full((B, C, Hkv, D), np.nan)
     st = status_tensor()
     scale = 0.1
     for s in range(steps):
@@ -97,6 +100,12 @@ def test_ring_append_then_decode_follows_the_history():
         vn = vh[:, p0:p0 + chunk].contiguous()
         binding.lat_kv_append_ring(binding.LAT_BF16, kr, vr, Hkv * D, D, C * Hkv * D, C, kn, vn,
                                    Hkv * D, pos, chunk, B, Hkv, D, st)
+        ok_k, ok_v = oracle.kv_append_ring(
+            ok_k, ok_v, kn.view(B, chunk, Hkv, D).cpu().float().numpy(),
+            vn.view(B, chunk, Hkv, D).cpu().float().numpy(), [p0] * B)
+        torch.cuda.synchronize()
+        assert_bits_equal(kr.view(B, C, Hkv, D), ok_k, "K ring after append %d" % s)
+        assert_bits_equal(vr.view(B, C, Hkv, D), ok_v, "V ring after append %d" % s)
         n = p0 + chunk
         lens_t = torch.full((B,), n, dtype=torch.int32, device="cuda")
         out, lse = run_ring(q, kr, vr, C, lens_t, total, B, Hq, Hkv, D, Wn, scale, "bf16")
@@ -107,3 +116,36 @@ def test_ring_append_then_decode_follows_the_history():
         compare(out, ref, "bf16", "step %d (length %d)" % (s, n), lse, ref_lse)
     # every ring row was written by the last append or an earlier one, none left NaN
     assert not torch.isnan(kr.float()).any()
+
+
+@pytest.mark.parametrize("dtype,head_major", [("bf16", False), ("f32", False), ("bf16", True)])
+def test_ring_append_bit_exact(dtype, head_major):
+    """lat_kv_append_ring against the oracle's ring copy, bit for bit in both caches:
+    sequences at different positions (one chunk wrapping past the end of the ring, one
+    starting exactly on a multiple of it), token-major and head-major cache layouts."""
+    B, Hkv, D, C, n_new = 3, 2, 64, 40, 9
+    pos = [35, 80, 3]  # 35..43 wraps; 80 = 2C lands on row 0
+    if head_major:  # [B, Hkv, C, D]: rows D apart, heads C*D apart
+        rs, hs, ss = D, C * D, Hkv * C * D
+    else:           # [B, C, Hkv*D]
+        rs, hs, ss = Hkv * D, D, C * Hkv * D
+    tdt = W.torch_dtype(dtype)
+    kc = torch.full((B * ss,), float("nan"), dtype=tdt, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    kn = W.normal((B * n_new, Hkv * D), dtype=dtype, device="cuda", seed=21, role="k")
+    vn = W.normal((B * n_new, Hkv * D), dtype=dtype, device="cuda", seed=21, role="v")
+    st = status_tensor()
+    binding.lat_kv_append_ring(DT[dtype], kc, vc, rs, hs, ss, C, kn, vn, Hkv * D,
+                               torch.tensor(pos, dtype=torch.int32, device="cuda"), n_new, B,
+                               Hkv, D, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+    def as_rows(t):  # [B, C, Hkv, D] whatever the layout
+        v = t.view(B, Hkv, C, D).permute(0, 2, 1, 3) if head_major else t.view(B, C, Hkv, D)
+        return v
+    empty = np.full((B, C, Hkv, D), np.nan)
+    ok_k, ok_v = oracle.kv_append_ring(empty, empty, kn.view(B, n_new, Hkv, D).cpu().float().numpy(),
+                                       vn.view(B, n_new, Hkv, D).cpu().float().numpy(), pos)
+    assert_bits_equal(as_rows(kc), ok_k, "K ring")
+    assert_bits_equal(as_rows(vc), ok_v, "V ring")
