@@ -4,20 +4,27 @@
                     [--workload NAME] [--no-extra] [--no-cpu]
 
 A step is one pass of the attention hot path over one batch of synthetic input.  The
-headline workload is the Qwen3-0.6B-shaped bf16 prefill (batch 8, 512 tokens, 16 query
-heads, 8 KV heads, head_dim 64, causal) read with row strides from one packed
-[4096, 2048] QKV buffer.  Each timed step is bracketed by CUDA events on the launching
-stream; before every step a 256 MiB write and a 256 MiB read leave L2 cold and clean.
+headline workload is the largest configuration that fits one GPU: the Gemma-4 global
+attention layer (16 query heads over 2 KV heads, head_dim 512), as a causal bf16 prefill
+of 8192 tokens; the same layer's decode step (8 sequences at 32768 cached tokens) is
+reported beside it under "decode".  Each timed step is bracketed by CUDA events on the
+launching stream; before every step a 256 MiB write and a 256 MiB read leave L2 cold and
+clean.
 
-`value` is TFLOP/s of algorithmic work (4*D FLOPs per visible query-key pair per head).
-`e2e` runs the steps through the C ABI from pinned host buffers: every step uploads its
-inputs and downloads its output and lse, pipelined over two buffer sets on three streams.
-`roofline` rates the prefill kernel against the HBM roofline (this workload's arithmetic
-intensity is below the ridge point).  `workloads` adds the other named shapes (Gemma-4
-sliding/global and Gemma-2 softcap prefill, chunked prefill on a cache, the three decode
-shapes, the attention-input producer), each rated against its own roofline.
-`cpu_baseline` is the fp64 oracle timed on the host cores.  With --impl reference the
-oracle itself is the timed arm.  --workload NAME makes any named workload the timed one.
+`value` is TFLOP/s of algorithmic work (4*D FLOPs per visible query-key pair per head);
+decode values are GB/s of K/V read (each cached element counted once per KV head).
+`e2e` runs the steps through the C ABI from pinned host buffers: a prefill step uploads
+Q/K/V and downloads the output and lse; a decode step uploads the query, the new K/V row
+and the lengths, appends the row into the device-resident cache, decodes and downloads
+the output and lse.  Steps are pipelined over two buffer sets on three streams.
+`roofline` rates the timed kernel against the tensor (prefill) or HBM (decode) roofline
+of MEASURED_PEAKS.json.  `workloads` adds the other named shapes, each against its own
+roofline, plus the tiny fp32 case (prefill, append, decode) in microseconds.
+`cpu_baseline` is the fp64 oracle on the host cores over a deterministic sample (query
+rows for prefill, sequences for decode), whose exact share of the algorithmic work is
+known, so the sample's throughput is the oracle's throughput on the whole workload.
+With --impl reference the oracle itself is the timed arm.  --workload NAME makes any
+named workload the timed one.
 
 Multi-GPU runs (torchrun) are independent replicas of the same workload (the path has no
 exchange step); every rank times its own steps and the slowest rank sets the time.
@@ -43,7 +50,8 @@ import torch  # noqa: E402
 import workloads as W  # noqa: E402
 
 METRIC = "GQA attention prefill TFLOP/s and decode KV GB/s, % of GB300 roofline"
-HEADLINE = "qwen3_0.6b_prefill"
+HEADLINE = "gemma4_global_prefill"
+COMPANION = "gemma4_global_decode"   # the same layer's decode step, reported beside it
 FLUSH_BYTES = 256 << 20
 L2_NOTE = ("flushed before every timed step: a 256 MiB write, then a 256 MiB read that "
            "leaves no dirty lines to write back during the step")
@@ -376,10 +384,21 @@ class DecodeStep:
             raise RuntimeError("device status %s" % self.b.lat_status_string(st))
 
 
-def measure_extra(device, flush, stream, peaks, reps=20):
+def prefill_bound(wl, peaks):
+    """'tensor' when the workload's arithmetic intensity is above the ridge point of the
+    measured peaks, else 'hbm'."""
+    flops, bytes_, _ = prefill_work(wl)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return "hbm" if flops / bytes_ < ridge else "tensor"
+
+
+def measure_extra(device, flush, stream, peaks, reps=20, skip=()):
     """The other named workloads, each against its own roofline."""
     res = {}
-    for name in ("gemma4_sliding_prefill", "gemma4_global_prefill", "gemma2_softcap_prefill"):
+    for name in ("gemma4_sliding_prefill", "qwen3_0.6b_prefill", "gemma2_softcap_prefill",
+                 "gemma4_global_prefill"):
+        if name in skip:
+            continue
         wl = W.WORKLOADS[name]
         step = PrefillStep(wl, device)
         for _ in range(3):
@@ -390,7 +409,9 @@ def measure_extra(device, flush, stream, peaks, reps=20):
         t = statistics.mean(ms) / 1e3
         tf = flops / t / 1e12
         res[name] = {"kind": "prefill", "ms": statistics.mean(ms), "tflops": tf,
-                     "bound": "tensor", "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                     "gbs": bytes_ / t / 1e9, "bound": prefill_bound(wl, peaks),
+                     "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                     "frac_of_hbm_peak": bytes_ / t / 1e9 / peaks["hbm_gbs"],
                      "gflop": flops / 1e9}
         del step
         torch.cuda.empty_cache()
@@ -424,7 +445,10 @@ def measure_extra(device, flush, stream, peaks, reps=20):
                      "mbytes": bytes_ / 1e6}
         del step
         torch.cuda.empty_cache()
-    for name in ("decode_b32_h32_kv8_d128", "gemma4_global_decode", "gemma4_sliding_decode_ring"):
+    for name in ("decode_b32_h32_kv8_d128", "gemma4_sliding_decode_ring",
+                 "decode_b1_kv2_d128_128k", "gemma4_global_decode"):
+        if name in skip:
+            continue
         wl = W.WORKLOADS[name]
         step = DecodeStep(wl, device)
         for _ in range(3):
@@ -439,9 +463,9 @@ def measure_extra(device, flush, stream, peaks, reps=20):
                      "tflops": flops / t / 1e12}
         del step
         torch.cuda.empty_cache()
-    # the headline with a warm L2: a burst of back-to-back steps between two events (its
-    # 25 MB of inputs and outputs stay in the 129 MB L2)
-    wl = W.WORKLOADS[HEADLINE]
+    # the Qwen3-shaped prefill with a warm L2: a burst of back-to-back steps between two
+    # events (its 25 MB of inputs and outputs stay in the 129 MB L2)
+    wl = W.WORKLOADS["qwen3_0.6b_prefill"]
     step = PrefillStep(wl, device)
     for _ in range(3):
         step()
@@ -456,13 +480,71 @@ def measure_extra(device, flush, stream, peaks, reps=20):
     step.check_status()
     flops, bytes_, _ = prefill_work(wl)
     t = s0.elapsed_time(s1) / n / 1e3
-    res[HEADLINE + "_warm_l2"] = {"kind": "prefill", "ms": t * 1e3, "tflops": flops / t / 1e12,
-                                  "bound": "latency", "gbs": bytes_ / t / 1e9,
-                                  "note": "no flush: back-to-back steps, inputs resident in L2"}
+    res[wl.name + "_warm_l2"] = {"kind": "prefill", "ms": t * 1e3, "tflops": flops / t / 1e12,
+                                 "bound": "latency", "gbs": bytes_ / t / 1e9,
+                                 "note": "no flush: back-to-back steps, inputs resident in L2"}
     del step
     torch.cuda.empty_cache()
     # KV append of one new row per sequence into the decode cache shape (timed on its own)
     res.update(measure_append(device, flush, stream, reps))
+    res.update(measure_tiny(device, flush, stream, reps))
+    return res
+
+
+def measure_tiny(device, flush, stream, reps):
+    """The tiny fp32 case in microseconds: a causal prefill of 64 tokens (4 query heads, 2
+    KV heads, head_dim 64), the append of token 63 into a 64-slot cache holding tokens
+    0..62, then one decode step at kv_len 64 -- three launches per step, and each alone."""
+    from gqa_attention_lat_gb300 import binding
+    pw = W.WORKLOADS["tiny_f32_prefill"]
+    B, S, Hq, Hkv, D = pw.B, pw.S, pw.Hq, pw.Hkv, pw.D
+    inp = W.prefill_inputs(B, S, S, Hq, Hkv, D, dtype="f32", device=device)
+    out = torch.empty((S, Hq * D), dtype=torch.float32, device=device)
+    lse = torch.empty((S, Hq), dtype=torch.float32, device=device)
+    cap = S
+    kc = torch.zeros((1, cap, Hkv * D), dtype=torch.float32, device=device)
+    vc = torch.zeros_like(kc)
+    kc[0, :S - 1] = inp.k[:S - 1]
+    vc[0, :S - 1] = inp.v[:S - 1]
+    pos = torch.tensor([S - 1], dtype=torch.int32, device=device)
+    lens = torch.tensor([S], dtype=torch.int32, device=device)
+    q_last = inp.q[S - 1:].contiguous()
+    dout = torch.empty((1, Hq * D), dtype=torch.float32, device=device)
+    dlse = torch.empty((1, Hq), dtype=torch.float32, device=device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def prefill():
+        binding.lat_attn_prefill(binding.LAT_F32, inp.q, inp.q.stride(0), inp.k,
+                                 inp.k.stride(0), inp.v, inp.v.stride(0), out, out.stride(0),
+                                 lse, B, S, S, Hq, Hkv, D, True, 0, pw.scale, st)
+
+    def append():
+        binding.lat_kv_append(binding.LAT_F32, kc, vc, Hkv * D, D, cap * Hkv * D, cap,
+                              inp.k[S - 1:], inp.v[S - 1:], inp.k.stride(0), pos, 1, 1, Hkv,
+                              D, st)
+
+    def decode():
+        binding.lat_attn_decode(binding.LAT_F32, q_last, q_last.stride(0), kc, vc, Hkv * D, D,
+                                cap * Hkv * D, lens, cap, dout, dout.stride(0), dlse, 1, Hq,
+                                Hkv, D, 0, pw.scale, None, 0, st)
+
+    def all3():
+        prefill()
+        append()
+        decode()
+    res = {}
+    for name, fn in (("tiny_f32_prefill_append_decode", all3), ("tiny_f32_prefill", prefill),
+                     ("tiny_f32_append", append), ("tiny_f32_decode", decode)):
+        for _ in range(3):
+            fn()
+        ms = time_steps(fn, reps, flush, stream)
+        res[name] = {"kind": "tiny_f32", "us": statistics.mean(ms) * 1e3,
+                     "us_median": statistics.median(ms) * 1e3, "bound": "latency",
+                     "launches": 3 if fn is all3 else 1,
+                     "note": "B1 S64 Hq4 Hkv2 D64 fp32, L2 flushed; event-timed, including "
+                             "the launch floor"}
+    if int(st.item()) != 0:
+        raise RuntimeError("device status %s" % binding.lat_status_string(int(st.item())))
     return res
 
 
@@ -492,49 +574,21 @@ def measure_append(device, flush, stream, reps):
                                        "note": "one new row per sequence, L2 flushed"}}
 
 
-def e2e_measure(step, steps, stream):
-    """Host buffers through the C ABI: every step uploads its inputs from pinned host
-    memory, runs, and downloads its outputs (and lse) into pinned host memory.  Steps are
-    pipelined over two buffer sets on three streams (upload, compute, download), so the
+def pipelined_e2e(hosts, out_like, run, steps, stream):
+    """Time `steps` end-to-end steps from pinned host buffers: each step uploads `hosts`
+    into one of two device buffer sets, calls run(dev_inputs, dev_outputs) on `stream`,
+    and downloads the outputs (shaped like `out_like`) into pinned host memory.  Steps
+    are pipelined over the two sets on three streams (upload, compute, download), so the
     upload of step i+1 and the download of step i-1 overlap the kernels of step i, as a
     serving loop over independent batches would run.  Returns (ms per step, h2d bytes,
     d2h bytes), the time being the whole run's span divided by the steps."""
-    if isinstance(step, PrefillStep):
-        wl, inp = step.wl, step.inp
-        if inp.packed is not None:
-            parents = [inp.packed]
-        else:
-            parents = [inp.q.contiguous(), inp.k.contiguous(), inp.v.contiguous()]
-        out_names = ("out", "lse")
-    elif isinstance(step, PrefillCachedStep):
-        d = step.di
-        parents = [step.q, d.k_cache, d.v_cache]
-        out_names = ("out", "lse")
-    elif isinstance(step, ProducerStep):
-        parents = [step.qkv]
-        out_names = ("q_out",)  # the cache rows stay on the device for the attention kernels
-    else:
-        d = step.di
-        parents = [d.q, d.k_cache, d.v_cache, d.kv_lens]
-        out_names = ("out", "lse")
-    hosts = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in parents]
-    for h, p in zip(hosts, parents):
-        h.copy_(p.cpu())
     nbuf = 2
-    devs = [[torch.empty_like(p) for p in parents] for _ in range(nbuf)]
-    outs = [[torch.empty_like(getattr(step, n)) for n in out_names] for _ in range(nbuf)]
-    host_outs = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs[0]]
+    devs = [[torch.empty(h.shape, dtype=h.dtype, device=stream.device) for h in hosts]
+            for _ in range(nbuf)]
+    outs = [[torch.empty_like(o) for o in out_like] for _ in range(nbuf)]
+    host_outs = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in out_like]
                  for _ in range(nbuf)]
-
-    def args_of(dv):
-        if isinstance(step, PrefillStep) and step.inp.packed is not None:
-            qw, kw = step.wl.Hq * step.wl.D, step.wl.Hkv * step.wl.D
-            buf = dv[0]
-            return (buf[:, :qw], buf[:, qw:qw + kw], buf[:, qw + kw:])
-        return tuple(dv)
-
     s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
-    keep = {n: getattr(step, n) for n in out_names}
     ev = lambda: torch.cuda.Event()
     up_done = [ev() for _ in range(nbuf)]
     run_done = [ev() for _ in range(nbuf)]
@@ -552,9 +606,7 @@ def e2e_measure(step, steps, stream):
         stream.wait_event(up_done[k])
         if used[k]:
             stream.wait_event(down_done[k])       # step i-2's outputs are downloaded
-        for n, o in zip(out_names, outs[k]):
-            setattr(step, n, o)
-        step(*args_of(devs[k]))
+        run(devs[k], outs[k])
         run_done[k].record(stream)
         with torch.cuda.stream(s_down):
             s_down.wait_event(run_done[k])
@@ -563,88 +615,219 @@ def e2e_measure(step, steps, stream):
             down_done[k].record(s_down)
         used[k] = True
 
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_up)
+    s_down.wait_stream(s_up)
+    stream.wait_stream(s_up)
+    for i in range(steps):
+        one(i)
+    s_up.wait_stream(s_down)
+    s_up.wait_stream(stream)
+    t1.record(s_up)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    d2h = sum(o.numel() * o.element_size() for o in host_outs[0])
+    return ms, h2d, d2h
+
+
+def pinned(t):
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t.cpu())
+    return h
+
+
+def e2e_measure(step, steps, stream):
+    """The step through the C ABI from pinned host buffers (see pipelined_e2e).
+
+    Prefill: every step uploads Q/K/V (the packed QKV buffer when the workload has one)
+    and downloads the output and lse.  Chunked prefill: the query chunk and the caches.
+    Producer: the fused QKV rows up, the attention input down (the cache rows stay on the
+    device for the attention kernels).  Decode: the cache is device-resident state; every
+    step uploads the query, the step's new K/V row, its cache position and the lengths,
+    appends the row (lat_kv_append, or lat_kv_append_ring for a ring cache), decodes and
+    downloads the output and lse."""
+    b = step.b
+    if isinstance(step, DecodeStep):
+        wl, d = step.wl, step.di
+        lens = d.kv_lens.long()
+        rows = torch.arange(wl.B, device=lens.device)
+        slot = (lens - 1) % wl.ring if wl.ring else lens - 1
+        # the new row re-writes the cache row it lands on, so the cache stays unchanged
+        k_new = d.k_cache[rows, slot].contiguous()
+        v_new = d.v_cache[rows, slot].contiguous()
+        pos = (d.kv_lens - 1).to(torch.int32)
+        hosts = [pinned(x) for x in (d.q, k_new, v_new, pos, d.kv_lens)]
+        row_w = wl.Hkv * wl.D
+
+        def run(dv, outs):
+            q, kn, vn, ps, kl = dv
+            if wl.ring:
+                b.lat_kv_append_ring(step.dt, d.k_cache, d.v_cache, row_w, wl.D,
+                                     wl.L * row_w, wl.ring, kn, vn, row_w, ps, 1, wl.B,
+                                     wl.Hkv, wl.D, step.status)
+            else:
+                b.lat_kv_append(step.dt, d.k_cache, d.v_cache, row_w, wl.D, wl.L * row_w,
+                                wl.L, kn, vn, row_w, ps, 1, wl.B, wl.Hkv, wl.D, step.status)
+            step.out, step.lse = outs
+            step(q, d.k_cache, d.v_cache, kl)
+        out_like = [step.out, step.lse]
+    else:
+        if isinstance(step, PrefillStep):
+            inp = step.inp
+            parents = ([inp.packed] if inp.packed is not None else
+                       [inp.q.contiguous(), inp.k.contiguous(), inp.v.contiguous()])
+            out_names = ("out", "lse")
+        elif isinstance(step, PrefillCachedStep):
+            parents = [step.q, step.di.k_cache, step.di.v_cache]
+            out_names = ("out", "lse")
+        else:  # ProducerStep
+            parents = [step.qkv]
+            out_names = ("q_out",)
+        hosts = [pinned(p) for p in parents]
+        out_like = [getattr(step, n) for n in out_names]
+
+        def run(dv, outs):
+            for n, o in zip(out_names, outs):
+                setattr(step, n, o)
+            if isinstance(step, PrefillStep) and step.inp.packed is not None:
+                qw, kw = step.wl.Hq * step.wl.D, step.wl.Hkv * step.wl.D
+                buf = dv[0]
+                step(buf[:, :qw], buf[:, qw:qw + kw], buf[:, qw + kw:])
+            else:
+                step(*dv)
+    keep = {n: getattr(step, n) for n in ("out", "lse", "q_out") if hasattr(step, n)}
     try:
-        for i in range(3):
-            one(i)
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(s_up)
-        s_down.wait_stream(s_up)
-        stream.wait_stream(s_up)
-        for i in range(steps):
-            one(i)
-        s_up.wait_stream(s_down)
-        s_up.wait_stream(stream)
-        t1.record(s_up)
-        torch.cuda.synchronize()
+        return pipelined_e2e(hosts, out_like, run, steps, stream)
     finally:
         for n, o in keep.items():
             setattr(step, n, o)
-    ms = t0.elapsed_time(t1) / steps
-    h2d = sum(h.numel() * h.element_size() for h in hosts)
-    d2h = sum(h.numel() * h.element_size() for h in host_outs[0])
-    return ms, h2d, d2h
 
 
 # ------------------------------------------------------------------------------ CPU arm
 
-def oracle_pass(wl, inp_cpu, threads, rows=None):
-    import oracle
-    return oracle.prefill(inp_cpu.heads("q"), inp_cpu.heads("k"), inp_cpu.heads("v"),
-                          causal=wl.causal, window=wl.window, scale=wl.scale, rows=rows,
-                          threads=threads)
+def row_pairs(wl, rows):
+    """Visible (query, key) pairs of each flattened query row r = b*S + i, per head."""
+    i = np.asarray(rows, dtype=np.int64) % wl.S
+    p = i + (wl.L - wl.S)
+    hi = np.minimum(wl.L, p + 1) if wl.causal else np.full(i.shape, wl.L, dtype=np.int64)
+    lo = np.maximum(0, p - wl.window + 1) if wl.window > 0 else np.zeros(i.shape, np.int64)
+    return np.maximum(hi - lo, 0)
 
 
-def cpu_baseline(wl, seconds=8.0):
-    """The oracle as it stands, on the host cores, over whole passes of the workload
-    (repeated until `seconds` of CPU time have run)."""
-    import oracle
-    oracle.build_library()
-    threads = oracle.default_threads()
-    inp = W.prefill_inputs(wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, dtype=wl.dtype, device="cpu",
-                           packed=wl.packed, k_mul=wl.k_mul)
-    flops, _, _ = prefill_work(wl)
+class OracleSample:
+    """A deterministic sample of one workload for the fp64 oracle, with the exact share
+    of the workload's algorithmic work it carries.
+
+    Prefill: the query rows of W.sample_rows (the first and last 4 rows of every
+    sequence, the rows around the window edge, `n_random` seeded rows), every head;
+    work = 4*D*Hq * (visible pairs of those rows).  Decode: the first `n_seq` sequences
+    at their drawn lengths, every head; work = their visible K/V bytes.  The inputs are
+    converted to float64 once, before any timing."""
+
+    def __init__(self, wl, n_random=256, n_seq=4):
+        import oracle
+        oracle.build_library()
+        self.oracle = oracle
+        self.wl = wl
+        self.threads = oracle.default_threads()
+        if wl.kind in ("prefill", "prefill_cached"):
+            inp = W.prefill_inputs(wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, dtype=wl.dtype,
+                                   device="cpu", k_mul=wl.k_mul)
+            self.q, self.k, self.v = (np.ascontiguousarray(inp.heads(x).double().numpy())
+                                      for x in ("q", "k", "v"))
+            extra = (wl.window - 1, wl.window, wl.window + 1) if wl.window > 0 else ()
+            self.rows = W.sample_rows(wl.B * wl.S, wl.S, extra=extra, n_random=n_random)
+            pairs = int(row_pairs(wl, self.rows).sum())
+            total = visible_pairs(wl.S, wl.L, wl.causal, wl.window) * wl.B
+            self.work = 4.0 * wl.D * wl.Hq * pairs / 1e12          # TFLOP
+            self.unit = "TFLOP/s"
+            self.share = pairs / total
+            self.what = ("%d of %d query rows x %d heads (%d of %d visible pairs per head)"
+                         % (len(self.rows), wl.B * wl.S, wl.Hq, pairs, total))
+        else:
+            if wl.ring:
+                lens = W.ring_decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, 1, wl.max_len).kv_lens
+            else:
+                lens = W.decode_inputs(wl.B, 1, 1, 8, max(wl.L, 1), kv_lens=wl.kv_lens,
+                                       nan_fill=False).kv_lens
+            lens = [int(x) for x in lens.tolist()]
+            vis = [min(n, wl.window) if wl.window > 0 else n for n in lens]
+            n = min(n_seq, wl.B)
+            self.vis = vis[:n]
+            mx = max(max(self.vis), 1)
+            g = np.random.default_rng(W.BASE_SEED)
+            self.q = g.standard_normal((n, wl.Hq, wl.D))
+            self.kc = g.standard_normal((n, mx, wl.Hkv, wl.D))
+            self.vc = g.standard_normal((n, mx, wl.Hkv, wl.D))
+            es = 2 if wl.dtype == "bf16" else 4
+            sample_keys = sum(self.vis)
+            self.work = sample_keys * wl.Hkv * wl.D * 2 * es / 1e9    # GB of K/V
+            self.unit = "GB/s"
+            self.share = sample_keys / max(sum(vis), 1)
+            self.what = ("%d of %d sequences (%d of %d visible keys) x %d KV heads"
+                         % (n, wl.B, sample_keys, sum(vis), wl.Hkv))
+
+    def run(self):
+        wl, o = self.wl, self.oracle
+        if wl.kind in ("prefill", "prefill_cached"):
+            o.prefill(self.q, self.k, self.v, causal=wl.causal, window=wl.window,
+                      scale=wl.scale, rows=self.rows, threads=self.threads,
+                      softcap=wl.softcap)
+        else:
+            o.decode(self.q, self.kc, self.vc, self.vis, window=0, scale=wl.scale,
+                     threads=self.threads)
+
+
+def cpu_baseline(wl, seconds=10.0):
+    """The oracle as it stands, on all host cores, over passes of a fixed sample of the
+    workload (repeated until `seconds` have run)."""
+    smp = OracleSample(wl)
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle_pass(wl, inp, threads)
+        smp.run()
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": flops * n / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "sample": "%d full passes of %s (fp64 oracle, %d threads, %.1f s)"
-            % (n, wl.name, threads, dt)}
+    value = smp.work * n / dt
+    return {"value": value, "unit": smp.unit, "cores": smp.threads, "kind": "oracle",
+            "sample": "%d passes over %s of %s (fp64 oracle, %d threads, %.1f s); the sample "
+                      "is %.4f of the workload's work, so a whole pass would take %.1f s"
+                      % (n, smp.what, wl.name, smp.threads, dt, smp.share,
+                         dt / n / smp.share)}
 
 
 def run_reference(args, rank, world):
-    """--impl reference: the oracle is the timed arm (rank 0 only)."""
+    """--impl reference: the oracle is the timed arm (rank 0 only); each step is one pass
+    over the workload's oracle sample."""
     if rank != 0:
         return
-    import oracle
-    oracle.build_library()
     wl = W.WORKLOADS[args.workload]
-    threads = oracle.default_threads()
-    inp = W.prefill_inputs(wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, dtype=wl.dtype, device="cpu",
-                           packed=wl.packed, k_mul=wl.k_mul)
-    flops, _, _ = prefill_work(wl)
+    smp = OracleSample(wl, n_random=128)  # a step of a second or two on 16 cores
     for _ in range(args.warmup):
-        oracle_pass(wl, inp, threads)
+        smp.run()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_pass(wl, inp, threads)
+        smp.run()
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
-    value = flops / (ms / 1e3) / 1e12
+    value = smp.work / (ms / 1e3)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": smp.unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": workload_config(wl),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": "each step is one full pass of %s" % wl.name},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "cpu_baseline": {"value": value, "unit": smp.unit, "cores": smp.threads,
+                         "kind": "oracle",
+                         "sample": "each step is one pass over %s of %s (%.4f of the "
+                                   "workload's work)" % (smp.what, wl.name, smp.share)},
+        "e2e": {"value": value, "unit": smp.unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -686,10 +869,72 @@ def workload_config(wl):
 
 # ------------------------------------------------------------------------------ main
 
+def kernel_info(wl, step, peaks):
+    """(algorithmic flops, bytes, work in the value's unit, unit, kernel name, roofline
+    bound, ncu summary name, kernel sources) of one workload."""
+    if wl.kind in ("prefill", "prefill_cached"):
+        flops, alg_bytes, _ = prefill_work(wl)
+        return (flops, alg_bytes, flops / 1e12, "TFLOP/s", "prefill_tc_kernel<%d>" % wl.D,
+                prefill_bound(wl, peaks), "prefill_tc_%s.md" % wl.name,
+                ["prefill_tc.cu", "device_common.cuh", "kernels.h"])
+    if wl.kind == "producer":
+        alg_bytes = producer_bytes(wl)
+        return (0.0, alg_bytes, alg_bytes / 1e9, "GB/s", "qkv_producer_fast<%d>" % wl.D, "hbm",
+                "qkv_producer_%s.md" % wl.name,
+                ["qkv_producer.cu", "device_common.cuh", "kernels.h"])
+    flops, alg_bytes, _ = decode_work(wl, step.di.kv_lens.cpu().tolist())
+    return (flops, alg_bytes, alg_bytes / 1e9, "GB/s", "decode_bf16_kernel<%d>" % wl.D, "hbm",
+            "decode_bf16_%s.md" % wl.name, ["decode_bf16.cu", "device_common.cuh", "kernels.h"])
+
+
+def measure_main(wl, device, flush, stream, peaks, peak_src, args, world, dist):
+    """Warm-up, the timed steps (max over ranks), roofline and e2e of one workload."""
+    step = {"prefill": PrefillStep, "prefill_cached": PrefillCachedStep,
+            "decode": DecodeStep, "producer": ProducerStep}[wl.kind](wl, device)
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    step.check_status()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms_steps = time_steps(step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    step.check_status()
+    flops, alg_bytes, work, unit, kernel, bound, profile, srcs = kernel_info(wl, step, peaks)
+    ms_total, _ = replica_throughput(sum(ms_steps), work, world, dist, device)
+    ms_per_step, value = replica_throughput(ms_total / args.steps, work, world)
+
+    e2e_ms, h2d, d2h = e2e_measure(step, args.steps, stream)
+    step.check_status()
+    e2e_ms, e2e_value = replica_throughput(e2e_ms, work, world, dist, device)
+
+    kernel_ms = statistics.mean(ms_steps)
+    tflops = flops / (kernel_ms / 1e3) / 1e12
+    if bound == "hbm":
+        achieved, peak, r_unit = alg_bytes / (kernel_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, r_unit = tflops, peaks["bf16_tflops"], "TFLOP/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": r_unit,
+                "frac": achieved / peak, "traffic": profile_traffic(profile, srcs),
+                "kernel": kernel, "peak_source": peak_src, "algorithmic_bytes": alg_bytes,
+                "algorithmic_flops": flops,
+                "tensor_frac": tflops / peaks["bf16_tflops"],
+                "hbm_frac": alg_bytes / (kernel_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    e2e = {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    # our kernels inside the timed region: one per step (the flush is torch's)
+    return {"value": value, "unit": unit, "ms_per_step": ms_per_step, "roofline": roofline,
+            "e2e": e2e, "gpu_launches": args.steps}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE)
@@ -730,83 +975,42 @@ def main():
     if wl.dtype != "bf16":
         raise SystemExit("bench workloads are bf16 (the fp32 shapes are parity cases)")
     flush = Flusher(device)
-    step = {"prefill": PrefillStep, "prefill_cached": PrefillCachedStep,
-            "decode": DecodeStep, "producer": ProducerStep}[wl.kind](wl, device)
     sampler = ClockSampler(local)
     sampler.start()
-    for _ in range(args.warmup):
-        flush()
-        step()
-    torch.cuda.synchronize()
-    step.check_status()
-
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ms_steps = time_steps(step, args.steps, flush, stream)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    step.check_status()
-    if wl.kind in ("prefill", "prefill_cached"):
-        flops, alg_bytes, _ = prefill_work(wl)
-        unit, work = "TFLOP/s", flops / 1e12
-        kernel = "prefill_tc_kernel<%d>" % wl.D
-        intensity = flops / alg_bytes
-        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        bound = "hbm" if intensity < ridge else "tensor"
-        profile, srcs = "prefill_tc_%s.md" % wl.name, ["prefill_tc.cu", "device_common.cuh", "kernels.h"]
-    elif wl.kind == "producer":
-        flops, alg_bytes = 0.0, producer_bytes(wl)
-        unit, work = "GB/s", alg_bytes / 1e9
-        kernel = "qkv_producer_fast<%d>" % wl.D
-        bound = "hbm"
-        profile, srcs = "qkv_producer_%s.md" % wl.name, ["qkv_producer.cu", "device_common.cuh", "kernels.h"]
-    else:
-        flops, alg_bytes, _ = decode_work(wl, step.di.kv_lens.cpu().tolist())
-        unit, work = "GB/s", alg_bytes / 1e9
-        kernel = "decode_bf16_kernel<%d>" % wl.D
-        bound = "hbm"
-        profile, srcs = "decode_bf16_%s.md" % wl.name, ["decode_bf16.cu", "device_common.cuh", "kernels.h"]
-    ms_total, _ = replica_throughput(sum(ms_steps), work, world, dist, device)
-    ms_per_step, value = replica_throughput(ms_total / args.steps, work, world)
-
-    e2e_ms, h2d, d2h = e2e_measure(step, args.steps, stream)
-    e2e_ms, e2e_value = replica_throughput(e2e_ms, work, world, dist, device)
-
+    head = measure_main(wl, device, flush, stream, peaks, peak_src, args, world, dist)
+    torch.cuda.empty_cache()
+    # the headline layer's decode step beside it
+    comp = None
+    if args.workload == HEADLINE:
+        cwl = W.WORKLOADS[COMPANION]
+        comp = measure_main(cwl, device, flush, stream, peaks, peak_src, args, world, dist)
+        comp["workload"] = workload_config(cwl)["workload"]
+        torch.cuda.empty_cache()
     extra = None
     if not args.no_extra:
-        del step
-        torch.cuda.empty_cache()
-        extra = measure_extra(device, flush, stream, peaks)
+        extra = measure_extra(device, flush, stream, peaks,
+                              skip=(args.workload, COMPANION if comp else None))
     clocks = sampler.stop()
 
-    cpu = None
-    if not args.no_cpu and rank == 0 and world == 1 and wl.kind == "prefill":
-        cpu = cpu_baseline(wl)
-
-    kernel_ms = statistics.mean(ms_steps)
-    if bound == "hbm":
-        achieved, peak, r_unit = alg_bytes / (kernel_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    if not args.no_cpu and rank == 0 and world == 1:
+        head["cpu_baseline"] = cpu_baseline(wl)
+        if comp is not None:
+            comp["cpu_baseline"] = cpu_baseline(W.WORKLOADS[COMPANION])
     else:
-        achieved, peak, r_unit = flops / (kernel_ms / 1e3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    traffic = profile_traffic(profile, srcs)
+        head["cpu_baseline"] = None
+
     line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16-rounded)",
         "config": workload_config(wl),
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": r_unit,
-                     "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
-                     "peak_source": peak_src, "algorithmic_bytes": alg_bytes,
-                     "algorithmic_flops": flops,
-                     "tensor_frac": (flops / (kernel_ms / 1e3) / 1e12) / peaks["bf16_tflops"]},
-        "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "roofline": head["roofline"],
+        "cpu_baseline": head["cpu_baseline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
         "clocks": clocks,
+        "decode": comp,
         "workloads": extra,
     }
     if rank == 0:

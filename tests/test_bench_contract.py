@@ -40,13 +40,41 @@ def test_every_workload_has_a_config_description():
         assert c["workload"].startswith(name) and c["l2"] and c["parallelism"] == "replicas"
 
 
-def test_algorithmic_work_of_the_headline():
+def test_algorithmic_work_of_the_prefills():
     """4 D Hq B flops per visible pair; Q + K + V read once, out + lse written once."""
-    wl = W.WORKLOADS[bench.HEADLINE]
+    wl = W.WORKLOADS["qwen3_0.6b_prefill"]
     flops, bytes_, pairs = bench.prefill_work(wl)
     assert pairs == 512 * 513 // 2
     assert flops == 4 * 64 * 16 * 8 * pairs
     assert bytes_ == 8 * 512 * (16 + 8 + 8) * 64 * 2 + 8 * 512 * 16 * 64 * 2 + 8 * 512 * 16 * 4
+    # the headline: the Gemma-4 global layer, B1 S8192 Hq16 Hkv2 D512 causal
+    wl = W.WORKLOADS[bench.HEADLINE]
+    assert (wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, wl.causal) == (1, 8192, 8192, 16, 2, 512, True)
+    flops, bytes_, pairs = bench.prefill_work(wl)
+    assert pairs == 8192 * 8193 // 2
+    assert flops == 4 * 512 * 16 * pairs  # 1.0996 TFLOP
+    assert bytes_ == 8192 * 16 * 512 * 2 * 2 + 2 * 8192 * 2 * 512 * 2 + 8192 * 16 * 4
+    # sliding window: 1024 keys per row once the window is full
+    wl = W.WORKLOADS["gemma4_sliding_prefill"]
+    assert bench.visible_pairs(8192, 8192, True, 1024) == 1024 * 1025 // 2 + (8192 - 1024) * 1024
+
+
+def test_decode_work_counts_each_kv_element_once_per_kv_head():
+    wl = W.WORKLOADS[bench.COMPANION]
+    flops, bytes_, keys = bench.decode_work(wl, [32768] * 8)
+    assert keys == 8 * 32768
+    assert bytes_ == keys * 2 * 512 * 2 * 2 + 8 * 16 * 512 * 2 * 2 + 8 * 16 * 4
+    assert flops == 4.0 * 512 * 16 * keys
+
+
+def test_oracle_sample_shares_are_exact():
+    """The CPU baseline's row sample carries exactly the visible pairs of its rows."""
+    wl = W.WORKLOADS["gemma4_sliding_prefill"]
+    rows = W.sample_rows(wl.B * wl.S, wl.S, extra=(1023, 1024, 1025), n_random=16)
+    per_row = bench.row_pairs(wl, rows)
+    for r, n in zip(rows, per_row):
+        i = r % wl.S
+        assert n == min(i + 1, 1024)
 
 
 import pytest  # noqa: E402
@@ -63,6 +91,11 @@ def test_ours_arm_prints_one_contract_line(cuda_device):
     d = json.loads(lines[0])
     assert BASE_KEYS <= set(d) and d["n_gpus"] == 1 and d["steps"] == 3
     assert d["value"] > 0 and d["gpu_launches"] == 3
+    assert d["config"]["workload"].startswith(bench.HEADLINE)
+    dec = d["decode"]
+    assert dec["workload"].startswith(bench.COMPANION) and dec["unit"] == "GB/s"
+    assert dec["value"] > 0 and dec["roofline"]["bound"] == "hbm"
+    assert dec["e2e"]["h2d_bytes_per_step"] > 0 and dec["e2e"]["d2h_bytes_per_step"] > 0
     rf = d["roofline"]
     assert rf["bound"] in ("hbm", "tensor") and 0 < rf["frac"] < 2 and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9

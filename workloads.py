@@ -246,6 +246,11 @@ WORKLOADS = {
     # (base 1e6), V copy, append into a token-major 4096-slot cache
     "qwen3_qkv_producer": Workload("qwen3_qkv_producer", "producer", "bf16", 8, 16, 8, 64,
                                    S=512, L=512, cap=4096),
+    # one long sequence: 16 query heads over 2 KV heads, head_dim 128, 131072 cached
+    # tokens -- two work units only, so the key stream must be cut finely to keep every
+    # SM busy
+    "decode_b1_kv2_d128_128k": Workload("decode_b1_kv2_d128_128k", "decode", "bf16", 1, 16, 2,
+                                        128, L=131072, kv_lens=131072),
     # chunked prefill against the decode cache: 512 new rows after 1536 cached keys, read
     # from a token-major 4096-slot cache (Qwen3-0.6B attention shape)
     "qwen3_chunked_prefill": Workload("qwen3_chunked_prefill", "prefill_cached", "bf16", 8, 16,
