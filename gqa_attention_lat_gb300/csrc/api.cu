@@ -165,14 +165,16 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
         return LAT_ERR_UNSUPPORTED;
     lat::PrefillTcArgs a{};
     a.wide = lat::prefill_tc_wide(head_dim, seq_len, kv_len, causal, window) ? 1 : 0;
-    const int bn = lat::prefill_tc_block_n(head_dim, a.wide != 0);
+    a.pair = lat::prefill_tc_pair(head_dim, n_heads, n_kv_heads) ? 1 : 0;
+    const int k_box = lat::prefill_tc_box_rows(head_dim, a.wide != 0, a.pair != 0, false);
+    const int v_box = lat::prefill_tc_box_rows(head_dim, a.wide != 0, a.pair != 0, true);
     // K/V maps span exactly kv_len rows per sequence: rows past it read as zeros, so cache
     // slots beyond the visible keys (which may hold anything) never reach the MMA
     if (!make_head_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, 128) ||
         !make_cache_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, kv.k_row, kv.k_head,
-                        kv.k_seq, bn, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
+                        kv.k_seq, k_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
         !make_cache_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, kv.v_row, kv.v_head,
-                        kv.v_seq, bn, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+                        kv.v_seq, v_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return LAT_ERR_CUDA;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.out_rs = out_rs;

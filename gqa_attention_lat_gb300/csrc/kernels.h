@@ -118,10 +118,15 @@ struct PrefillTcArgs {
     uint64_t timeout_ns;
     int test_skip_kv_load;         // test hook: never load KV tile 0 (forces a timeout)
     int wide;                      // head_dim 64: the 96-key-tile form (prefill_tc_wide)
+    int pair;                      // head_dim 512, even GQA group: the CTA-pair form
 };
 // the 96-key-tile form of head_dim 64 for long key ranges (a query tile visiting ~1K keys)
 bool prefill_tc_wide(int head_dim, int seq_len, int kv_len, int causal, int window);
 int prefill_tc_block_n(int head_dim, bool wide);  // keys per KV tile
+// head_dim 512 with an even number of query heads per KV head runs on CTA pairs
+bool prefill_tc_pair(int head_dim, int n_heads, int n_kv_heads);
+// rows of the K (v = false) or V (v = true) tensor-map box of the chosen form
+int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v);
 // work items of one prefill launch (query tile x head x output-column part); the kernel
 // numbers them in int32, so the host refuses shapes above kPrefillMaxItems
 int64_t prefill_tc_items(int batch, int n_heads, int head_dim, int seq_len);

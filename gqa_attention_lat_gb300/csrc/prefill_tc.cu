@@ -35,8 +35,17 @@
 //    in tensor memory is rare; the result is exact up to rounding because O and l always
 //    share the same reference maximum.
 //  * head_dim 80 runs as two chunks (64 + 16 live columns; the tensor map zero-fills
-//    columns past 80).  head_dim 512 splits O across two CTAs of 256 columns each (a
-//    128 x 512 fp32 accumulator alone would fill tensor memory); each recomputes S.
+//    columns past 80).  head_dim 512 splits O into two 256-column halves (a 128 x 512 fp32
+//    accumulator alone would fill tensor memory), each half an item of its own.
+//  * head_dim 512 with an even GQA group runs on CTA pairs (a 2-CTA cluster on the two SMs
+//    of a TPC, tcgen05 .cta_group::2): the pair takes one query tile of two query heads
+//    that share a KV head, CTA r holding head 2j+r's 128 query rows.  Each pair MMA is
+//    M = 256 (both heads' rows) x N = 128 keys, with every CTA holding only its 64 keys of
+//    the K tile and its 128 columns of the V tile, so a 128-key tile fits next to a
+//    128 x 512 query tile in shared memory and the S MMA runs at N = 128 (a single CTA
+//    could only afford N = 64, which the tensor pipe runs at about half rate).  The even
+//    CTA issues the MMAs; both CTAs' copies count on its barriers, and its commits arrive
+//    on the barriers of both.
 //  * Every mbarrier wait is bounded by a wall-clock budget; on expiry the CTA records
 //    LAT_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees tensor memory and exits.
 #include <math.h>
@@ -60,8 +69,9 @@ constexpr int kChunkCols = 64;       // head-dim columns per swizzled chunk (128
 constexpr uint32_t kTmemO = 0;       // O accumulator columns [0, kOCols)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D, bool W = false>
+template <int D, bool W = false, bool P = false>
 struct TcCfg {
+    static_assert(!P || D == 512, "the CTA-pair form exists for head_dim 512");
     static constexpr int kQkChunks = (D + kChunkCols - 1) / kChunkCols;   // Q/K chunks
     static constexpr int kKSteps = (D + 15) / 16;                          // S MMA k-steps
     // keys per tile; head_dim 64 takes 64-key tiles so that two CTAs fit one SM (256 tensor
@@ -69,18 +79,22 @@ struct TcCfg {
     // chain of S MMA, softmax and P.V leaves the SM idle, and a second CTA fills the gaps
     // W (head_dim 64 with long key ranges): 96-key tiles, which halve the per-tile fixed
     // costs where a query tile visits a thousand keys or more, still two CTAs per SM
-    static constexpr int kBN = D == 64 ? (W ? 96 : 64) : (D <= 256 ? 128 : 64);
+    // P (head_dim 512 on a CTA pair): 128-key tiles, 64 keys of K in each CTA
+    static constexpr int kBN = P ? 128 : (D == 64 ? (W ? 96 : 64) : (D <= 256 ? 128 : 64));
+    static constexpr int kKRows = P ? kBN / 2 : kBN;                       // K rows per CTA
     static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
     static constexpr uint32_t kTmemS = D == 64 ? 64 : 256;     // S buffers at kTmemS (+ BN)
     static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
-    static constexpr int kSplitO = D == 512 ? 2 : 1;                       // CTAs per O row
+    static constexpr int kSplitO = D == 512 ? 2 : 1;                       // O column halves
     static constexpr int kOCols = D / kSplitO;                             // O cols per CTA
-    static constexpr int kVChunks = (kOCols + kChunkCols - 1) / kChunkCols;
-    static constexpr int kChunkBytes = kBN * 128;                          // one [BN x 64] chunk
-    static constexpr int kKTileBytes = kQkChunks * kChunkBytes;
-    static constexpr int kVTileBytes = kVChunks * kChunkBytes;
-    static constexpr int kKStages = D == 64 ? (W ? 3 : 4) : (D <= 128 ? 3 : 1);
-    static constexpr int kVStages = D == 64 ? (W ? 3 : 4) : (D <= 128 ? 2 : 1);
+    static constexpr int kVCols = P ? kOCols / 2 : kOCols;                 // V cols per CTA
+    static constexpr int kVChunks = (kVCols + kChunkCols - 1) / kChunkCols;
+    static constexpr int kKChunkBytes = kKRows * 128;                      // [rows x 64] chunk
+    static constexpr int kVChunkBytes = kBN * 128;
+    static constexpr int kKTileBytes = kQkChunks * kKChunkBytes;
+    static constexpr int kVTileBytes = kVChunks * kVChunkBytes;
+    static constexpr int kKStages = P ? 1 : (D == 64 ? (W ? 3 : 4) : (D <= 128 ? 3 : 1));
+    static constexpr int kVStages = P ? 1 : (D == 64 ? (W ? 3 : 4) : (D <= 128 ? 2 : 1));
     static constexpr int kQBytes = kQkChunks * kBM * 128;
     static constexpr int kQStages = D <= 128 ? 2 : 1;   // the next item's Q loads early
     static constexpr int kBarBytes = 256 + 4 * kBM * 4;  // barriers + row exchange
@@ -152,6 +166,8 @@ __device__ __forceinline__ Band kv_band(int m0, int rows, int S, int L, int caus
 }
 
 // One unit of work: a 128-row query tile of one query head (and one O half for D = 512).
+// On a CTA pair the unit is the same tile of two query heads of one GQA group, CTA r
+// taking head 2j + r.
 struct Item {
     int b, h, half, m0, rows, hk;
     Band band;
@@ -159,17 +175,19 @@ struct Item {
 
 // Items are numbered heaviest first (latest query tiles, which see the most keys under a
 // causal mask), then by sequence and head.
-template <int D, bool W>
-__device__ __forceinline__ Item item_at(const PrefillTcArgs &a, int idx) {
-    using C = TcCfg<D, W>;
-    const int per_tile = a.batch * a.n_heads * C::kSplitO;
+template <int D, bool W, bool P>
+__device__ __forceinline__ Item item_at(const PrefillTcArgs &a, int idx, int rank) {
+    using C = TcCfg<D, W, P>;
+    const int head_slots = P ? a.n_heads / 2 : a.n_heads;  // heads, or head pairs
+    const int per_tile = a.batch * head_slots * C::kSplitO;
     const int n_mtiles = (a.seq_len + kBM - 1) / kBM;
     const int z = idx / per_tile, rem = idx % per_tile;
     const int mt = n_mtiles - 1 - z;
     Item it;
-    it.b = rem / (a.n_heads * C::kSplitO);
-    const int head_sel = rem % (a.n_heads * C::kSplitO);
-    it.h = head_sel / C::kSplitO;
+    it.b = rem / (head_slots * C::kSplitO);
+    const int head_sel = rem % (head_slots * C::kSplitO);
+    const int hs = head_sel / C::kSplitO;
+    it.h = P ? 2 * hs + rank : hs;
     it.half = head_sel % C::kSplitO;
     it.m0 = mt * kBM;
     it.rows = min(kBM, a.seq_len - it.m0);
@@ -186,16 +204,16 @@ __device__ __forceinline__ int item_index(int k, int c, int G, int n_items) {
     return idx < n_items ? idx : -1;
 }
 
-template <int D, bool W>
-__global__ void __launch_bounds__(kThreads, TcCfg<D, W>::kCtasPerSm)
+template <int D, bool W, bool P>
+__global__ void __launch_bounds__(kThreads, TcCfg<D, W, P>::kCtasPerSm)
 prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
-    using C = TcCfg<D, W>;
+    using C = TcCfg<D, W, P>;
     constexpr int BN = C::kBN;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    if (C::kSlack == 0 && smem != smem_raw) {  // no room to realign: refuse to run
-        if (threadIdx.x == 0) report_status(a.status, kErrCuda);
+    if (C::kSlack == 0 && smem != smem_raw) {  // no room to realign: refuse to run (both
+        if (threadIdx.x == 0) report_status(a.status, kErrCuda);  // CTAs of a pair alike)
         return;
     }
     unsigned char *sQ = smem;                                 // [kQStages] Q tiles
@@ -219,8 +237,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     float *xchg = reinterpret_cast<float *>(bars + 32);   // [2 parities][2 warpgroups][kBM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = a.batch * a.n_heads * C::kSplitO * ((a.seq_len + kBM - 1) / kBM);
-    const int cta = blockIdx.x, G = gridDim.x;
+    const int head_slots = P ? a.n_heads / 2 : a.n_heads;
+    const int n_items = a.batch * head_slots * C::kSplitO * ((a.seq_len + kBM - 1) / kBM);
+    // a pair walks its items together: the cluster is the unit of the schedule
+    const uint32_t rank = P ? cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int cta = P ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int G = P ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const uint64_t deadline = globaltimer_ns() + a.timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -228,7 +251,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
             mbar_init(&bar_s[i], 1);
-            mbar_init(&bar_p[i], kSoftmaxThreads);
+            // P: every softmax thread of both CTAs arrives on the even CTA's barrier
+            mbar_init(&bar_p[i], P ? 2 * kSoftmaxThreads : kSoftmaxThreads);
         }
         for (int q = 0; q < 4; ++q) mbar_init(&bar_x[q], 2);  // one arrival per warp
         mbar_init(bar_o, 1);
@@ -245,25 +269,43 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    if (warp == kMmaWarp) {  // whole warp: allocate tensor memory
-        tmem_alloc(tmem_slot, C::kTmemCols);
-        tmem_relinquish();
+    if (warp == kMmaWarp) {  // whole warp: allocate tensor memory (both CTAs of a pair)
+        if constexpr (P) {
+            tmem_alloc_pair(tmem_slot, C::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, C::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (P)
+        cluster_sync_all();  // the peer's barriers are initialised before any remote signal
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // waits on barriers the peer CTA (or the pair's MMAs) also signals
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) {
+        if constexpr (P)
+            return mbar_wait_bounded_cluster(bar, parity, abort_flag, deadline);
+        else
+            return mbar_wait_bounded(bar, parity, abort_flag, deadline);
+    };
 
     if (warp == kKProducerWarp || warp == kVProducerWarp) {
         // ------------------------------------------------------------ TMA producers
         // warp 8 loads each item's Q, then its K tiles; warp 9 loads its V tiles (this
         // item's O columns).  The rings run on across items.  One mbarrier per tile
-        // carries all of the tile's chunk copies.
+        // carries all of the tile's chunk copies.  On a pair, both CTAs' copies of a tile
+        // count on the even CTA's barrier, which that CTA arms for both.
         if (lane == 0) {
             const bool is_k = warp == kKProducerWarp;
             const int stages = is_k ? C::kKStages : C::kVStages;
             const int tile_bytes = is_k ? C::kKTileBytes : C::kVTileBytes;
+            const int chunk_bytes = is_k ? C::kKChunkBytes : C::kVChunkBytes;
             const int chunks = is_k ? C::kQkChunks : C::kVChunks;
+            const int arm = P ? 2 : 1;  // CTAs whose copies a barrier counts
             unsigned char *ring = is_k ? sK : sV;
             uint64_t *full = is_k ? k_full : v_full;
             uint64_t *empty = is_k ? k_empty : v_empty;
@@ -275,59 +317,93 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             for (int k = 0; ok; ++k) {
                 const int idx = item_index(k, cta, G, n_items);
                 if (idx < 0) break;
-                const Item it = item_at<D, W>(a, idx);
+                const Item it = item_at<D, W, P>(a, idx, rank);
                 if (is_k) {
                     const int qs = qi % C::kQStages;
-                    if (!mbar_wait_bounded(&q_empty[qs], ((qi / C::kQStages) & 1) ^ 1, abort_flag,
-                                           deadline)) {
+                    if (!wait_bar(&q_empty[qs], ((qi / C::kQStages) & 1) ^ 1)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&q_full[qs], C::kQBytes);
-                    for (int c = 0; c < C::kQkChunks; ++c)
-                        tma_load_4d(sQ + qs * C::kQBytes + c * kBM * 128, &a.tm_q, &q_full[qs],
-                                    c * kChunkCols, it.h, it.m0, it.b);
+                    if (leader) mbar_arrive_expect_tx(&q_full[qs], arm * C::kQBytes);
+                    for (int c = 0; c < C::kQkChunks; ++c) {
+                        unsigned char *dst = sQ + qs * C::kQBytes + c * kBM * 128;
+                        if constexpr (P)
+                            tma_load_4d_pair(dst, &a.tm_q, cluster_addr(&q_full[qs], 0),
+                                             c * kChunkCols, it.h, it.m0, it.b);
+                        else
+                            tma_load_4d(dst, &a.tm_q, &q_full[qs], c * kChunkCols, it.h, it.m0,
+                                        it.b);
+                    }
                     ++qi;
                 }
-                const int col0 = is_k ? 0 : it.half * C::kOCols;
+                // K: this CTA's rows of the tile (all of them, or its half on a pair); V: its
+                // columns of the item's O columns
+                const int col0 = is_k ? 0 : it.half * C::kOCols + (int)rank * C::kVCols;
+                const int row_off = is_k ? (int)rank * C::kKRows : 0;
                 for (int t = it.band.t_begin; t < it.band.t_end; ++t, ++g) {
                     const int s = g % stages;
-                    if (!mbar_wait_bounded(&empty[s], ((g / stages) & 1) ^ 1, abort_flag, deadline)) {
+                    if (!wait_bar(&empty[s], ((g / stages) & 1) ^ 1)) {
                         ok = false;
                         break;
                     }
                     if (is_k && a.test_skip_kv_load && g == 0) continue;  // test hook: never load
-                    mbar_arrive_expect_tx(&full[s], tile_bytes);
-                    for (int c = 0; c < chunks; ++c)
-                        tma_load_4d(ring + s * tile_bytes + c * C::kChunkBytes, tm, &full[s],
-                                    col0 + c * kChunkCols, it.hk, t * BN, it.b);
+                    if (leader) mbar_arrive_expect_tx(&full[s], arm * tile_bytes);
+                    for (int c = 0; c < chunks; ++c) {
+                        unsigned char *dst = ring + s * tile_bytes + c * chunk_bytes;
+                        if constexpr (P)
+                            tma_load_4d_pair(dst, tm, cluster_addr(&full[s], 0),
+                                             col0 + c * kChunkCols, it.hk, t * BN + row_off, it.b);
+                        else
+                            tma_load_4d(dst, tm, &full[s], col0 + c * kChunkCols, it.hk,
+                                        t * BN + row_off, it.b);
+                    }
                 }
             }
             // drain: every issued copy must land before the CTA may exit.  Fills go round
             // each ring in order, so slot s last held fill s + j*stages, the largest below
-            // the count issued.
+            // the count issued.  On a pair the even CTA's barriers count both CTAs' copies,
+            // and the odd CTA stays at the closing cluster barrier until the even one
+            // has drained.
             const uint64_t drain_deadline = globaltimer_ns() + 100000000ull;
             volatile int no_abort = 0;
-            for (int s = 0; s < stages; ++s)
-                if (s < g) {
-                    const int last = s + (g - 1 - s) / stages * stages;
-                    if (!(is_k && a.test_skip_kv_load && last == 0))
-                        mbar_wait_bounded(&full[s], (last / stages) & 1, &no_abort, drain_deadline);
-                }
-            if (is_k)
-                for (int s = 0; s < C::kQStages; ++s)
-                    if (s < qi) {
-                        const int last = s + (qi - 1 - s) / C::kQStages * C::kQStages;
-                        mbar_wait_bounded(&q_full[s], (last / C::kQStages) & 1, &no_abort,
-                                          drain_deadline);
+            if (leader) {
+                for (int s = 0; s < stages; ++s)
+                    if (s < g) {
+                        const int last = s + (g - 1 - s) / stages * stages;
+                        if (!(is_k && a.test_skip_kv_load && last == 0))
+                            mbar_wait_bounded(&full[s], (last / stages) & 1, &no_abort,
+                                              drain_deadline);
                     }
+                if (is_k)
+                    for (int s = 0; s < C::kQStages; ++s)
+                        if (s < qi) {
+                            const int last = s + (qi - 1 - s) / C::kQStages * C::kQStages;
+                            mbar_wait_bounded(&q_full[s], (last / C::kQStages) & 1, &no_abort,
+                                              drain_deadline);
+                        }
+            }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = instr_desc(kBM, BN, false);
-            constexpr uint32_t idesc_pv = instr_desc(kBM, C::kOCols, true);
+        // (on a pair, the even CTA's warp issues for both; the odd CTA's warp only waits
+        // for the last MMA before the tensor memory is freed)
+        if (lane == 0 && leader) {
+            constexpr int kM = P ? 2 * kBM : kBM;
+            constexpr uint32_t idesc_s = instr_desc(kM, BN, false);
+            constexpr uint32_t idesc_pv = instr_desc(kM, P ? 2 * C::kVCols : C::kOCols, true);
+            auto mma_ss = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
+                if constexpr (P) tc_mma_ss_pair(d, ad, bd, id, acc);
+                else tc_mma_ss(d, ad, bd, id, acc);
+            };
+            auto mma_ts = [&](uint32_t d, uint32_t at, uint64_t bd, uint32_t id, uint32_t acc) {
+                if constexpr (P) tc_mma_ts_pair(d, at, bd, id, acc);
+                else tc_mma_ts(d, at, bd, id, acc);
+            };
+            auto commit = [&](uint64_t *bar) {
+                if constexpr (P) tc_commit_pair(bar);
+                else tc_commit(bar);
+            };
             // Descriptors are built once; advancing an operand by B bytes adds B >> 4 to
             // the start-address field (all smem addresses here are below 256 KB, so the
             // 14-bit field never carries), which keeps the issue loop to a few
@@ -339,10 +415,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             for (int k = 0, qi = 0; ok; ++k, ++qi) {
                 const int idx = item_index(k, cta, G, n_items);
                 if (idx < 0) break;
-                const Item it = item_at<D, W>(a, idx);
+                const Item it = item_at<D, W, P>(a, idx, rank);
                 const int n_tiles = it.band.t_end - it.band.t_begin;
                 const int qs = qi % C::kQStages;
-                if (!mbar_wait_bounded(&q_full[qs], (qi / C::kQStages) & 1, abort_flag, deadline)) {
+                if (!wait_bar(&q_full[qs], (qi / C::kQStages) & 1)) {
                     ok = false;
                     break;
                 }
@@ -353,7 +429,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                         // S(g+t) = Q K^T into S buffer (g+t) % 2
                         const int gt = g + t;
                         const int s = gt % C::kKStages;
-                        if (!mbar_wait_bounded(&k_full[s], (gt / C::kKStages) & 1, abort_flag, deadline)) {
+                        if (!wait_bar(&k_full[s], (gt / C::kKStages) & 1)) {
                             ok = false;
                             break;
                         }
@@ -365,48 +441,53 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk) {
                                 if (c * 4 + kk < C::kKSteps)
-                                    tc_mma_ss(d_s, dq + (uint64_t)((c * kBM * 128 + kk * 32) >> 4),
-                                              dk + (uint64_t)((c * C::kChunkBytes + kk * 32) >> 4),
-                                              idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+                                    mma_ss(d_s, dq + (uint64_t)((c * kBM * 128 + kk * 32) >> 4),
+                                           dk + (uint64_t)((c * C::kKChunkBytes + kk * 32) >> 4),
+                                           idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
                             }
                         }
-                        tc_commit(&k_empty[s]);
-                        tc_commit(&bar_s[gt & 1]);
-                        if (t == n_tiles - 1) tc_commit(&q_empty[qs]);  // Q read for the last time
+                        commit(&k_empty[s]);
+                        commit(&bar_s[gt & 1]);
+                        if (t == n_tiles - 1) commit(&q_empty[qs]);  // Q read for the last time
                     }
                     if (t > 0) {
                         // O += P V for tile g+t-1: A = P from tensor memory (the S buffer it
                         // was computed from, 8 columns per 16 keys), B = V MN-major with its
-                        // 64-column atoms kChunkBytes apart, N = every O column of the item.
+                        // 64-column atoms kVChunkBytes apart, N = every O column of the item.
                         // The first group overwrites O: the previous item's epilogue read it
                         // before its softmax published this item's first P.
                         const int gp = g + t - 1;
                         const int s = gp % C::kVStages;
-                        if (!mbar_wait_bounded(&bar_p[gp & 1], (gp >> 1) & 1, abort_flag, deadline) ||
-                            !mbar_wait_bounded(&v_full[s], (gp / C::kVStages) & 1, abort_flag, deadline)) {
+                        if (!wait_bar(&bar_p[gp & 1], (gp >> 1) & 1) ||
+                            !wait_bar(&v_full[s], (gp / C::kVStages) & 1)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t dv = sw128_desc_mn(smem_u32(sV) + s * C::kVTileBytes, C::kChunkBytes);
+                        const uint64_t dv = sw128_desc_mn(smem_u32(sV) + s * C::kVTileBytes,
+                                                          C::kVChunkBytes);
                         const uint32_t p_tmem = tmem + C::kTmemS + (uint32_t)((gp & 1) * BN);
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
-                            tc_mma_ts(tmem + kTmemO, p_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
-                                      idesc_pv, (t > 1 || kk > 0) ? 1u : 0u);
-                        tc_commit(&v_empty[s]);
-                        tc_commit(bar_o);
+                            mma_ts(tmem + kTmemO, p_tmem + kk * 8, dv + (uint64_t)((kk * 2048) >> 4),
+                                   idesc_pv, (t > 1 || kk > 0) ? 1u : 0u);
+                        commit(&v_empty[s]);
+                        commit(bar_o);
                     }
                 }
                 if (!ok) break;
-                if (n_tiles == 0) tc_commit(&q_empty[qs]);  // nothing read this Q
-                tc_commit(o_full);  // the item's O is complete once every MMA above is
+                if (n_tiles == 0) commit(&q_empty[qs]);  // nothing read this Q
+                commit(o_full);  // the item's O is complete once every MMA above is
                 g += n_tiles;
             }
             // drain: all issued MMAs must finish before tensor memory is freed
-            tc_commit(bar_done);
+            commit(bar_done);
             volatile int no_abort = 0;
             mbar_wait_bounded(bar_done, 0, &no_abort, globaltimer_ns() + 100000000ull);
+        } else if (P && lane == 0) {
+            // the odd CTA of a pair: its tensor memory is written by the pair's MMAs
+            volatile int no_abort = 0;
+            mbar_wait_bounded_cluster(bar_done, 0, &no_abort, deadline + 100000000ull);
         }
         __syncwarp();
     } else {
@@ -425,11 +506,14 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         const float sl2 = capped ? 1.f : a.scale_log2;  // capped scores arrive pre-scaled
         const bool max_mode = sl2 >= 0.f;             // a negative scale flips max and min
         const float hide = max_mode ? -INFINITY : INFINITY;  // raw value that never wins
+        // P(g) ready: this CTA's barrier, or on a pair the even CTA's (which issues P.V)
+        const uint32_t bar_p_pair[2] = {P ? cluster_addr(&bar_p[0], 0) : 0u,
+                                        P ? cluster_addr(&bar_p[1], 0) : 0u};
         bool ok = true;
         int xn = 0;  // exchanges done (selects the exchange buffer and barrier phase)
         // tcgen05.ld/st are warp-collective, so a wait's outcome is made warp-uniform
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
-            const bool r = mbar_wait_bounded(bar, parity, abort_flag, deadline);
+            const bool r = wait_bar(bar, parity);
             return __all_sync(0xffffffffu, r) != 0;
         };
         // publish v for the partner warp and read the partner's value
@@ -447,7 +531,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         for (int k = 0; ok; ++k) {
             const int idx = item_index(k, cta, G, n_items);
             if (idx < 0) break;
-            const Item it = item_at<D, W>(a, idx);
+            const Item it = item_at<D, W, P>(a, idx, rank);
             const int n_tiles = it.band.t_end - it.band.t_begin;
             const int i = it.m0 + row;                       // query row within the sequence
             const int p = i + (a.kv_len - a.seq_len);        // its absolute position
@@ -555,7 +639,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                 l_part = l_part * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
                 m_ref = m_new;
                 tc_fence_before();
-                mbar_arrive(&bar_p[gt & 1]);
+                if constexpr (P)
+                    mbar_arrive_cluster(bar_p_pair[gt & 1]);
+                else
+                    mbar_arrive(&bar_p[gt & 1]);
             }
             if (!ok) break;
             g += n_tiles;
@@ -600,23 +687,68 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (P)
+        cluster_sync_all();  // neither CTA leaves while the pair's MMAs or copies may touch it
+    else
+        __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) report_status(a.status, kErrTimeout);
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::kTmemCols);
+        if constexpr (P)
+            tmem_dealloc_pair(tmem, C::kTmemCols);
+        else
+            tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
 template <int D, bool W = false>
 cudaError_t launch_d(const PrefillTcArgs &a, int num_sms, cudaStream_t s) {
     using C = TcCfg<D, W>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, W>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, W, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t n_items = (int64_t)a.batch * a.n_heads * C::kSplitO * ((a.seq_len + kBM - 1) / kBM);
     const int grid = (int)std::min<int64_t>(n_items, std::max(1, num_sms) * C::kCtasPerSm);
-    prefill_tc_kernel<D, W><<<grid, kThreads, C::kSmem, s>>>(a);
+    prefill_tc_kernel<D, W, false><<<grid, kThreads, C::kSmem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// The CTA-pair form: a persistent grid of as many 2-CTA clusters as fit the GPU at once
+// (one per TPC whose two SMs are both available), capped by the number of items.
+cudaError_t launch_pair_512(const PrefillTcArgs &a, cudaStream_t s) {
+    using C = TcCfg<512, false, true>;
+    auto kern = prefill_tc_kernel<512, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    static int clusters_per_dev[64] = {};  // co-resident clusters, asked once per device
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (clusters_per_dev[dev] == 0) {
+        int sms = 0, n = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        cfg.gridDim = dim3(2 * (sms / 2));
+        if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
+        clusters_per_dev[dev] = std::max(1, n);
+    }
+    const int64_t n_items = (int64_t)a.batch * (a.n_heads / 2) * C::kSplitO *
+                            ((a.seq_len + kBM - 1) / kBM);
+    const int clusters = (int)std::min<int64_t>(n_items, clusters_per_dev[dev]);
+    cfg.gridDim = dim3(2 * clusters);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -630,6 +762,10 @@ bool prefill_tc_wide(int head_dim, int seq_len, int kv_len, int causal, int wind
     return keys >= 1024.0;
 }
 
+bool prefill_tc_pair(int head_dim, int n_heads, int n_kv_heads) {
+    return head_dim == 512 && (n_heads / n_kv_heads) % 2 == 0;
+}
+
 int prefill_tc_block_n(int head_dim, bool wide) {
     switch (head_dim) {
         case 64: return wide ? TcCfg<64, true>::kBN : TcCfg<64>::kBN;
@@ -641,6 +777,11 @@ int prefill_tc_block_n(int head_dim, bool wide) {
     }
 }
 
+int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v) {
+    if (pair) return v ? TcCfg<512, false, true>::kBN : TcCfg<512, false, true>::kKRows;
+    return prefill_tc_block_n(head_dim, wide);
+}
+
 int64_t prefill_tc_items(int batch, int n_heads, int head_dim, int seq_len) {
     const int split = head_dim == 512 ? TcCfg<512>::kSplitO : 1;
     return (int64_t)batch * n_heads * split * ((seq_len + kBM - 1) / kBM);
@@ -650,6 +791,10 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t 
     if (a.seq_len == 0 || a.batch == 0) return cudaSuccess;
     if (prefill_tc_items(a.batch, a.n_heads, a.head_dim, a.seq_len) > kPrefillMaxItems)
         return cudaErrorInvalidValue;
+    if (a.pair) {
+        if (!prefill_tc_pair(a.head_dim, a.n_heads, a.n_kv_heads)) return cudaErrorInvalidValue;
+        return launch_pair_512(a, s);
+    }
     switch (a.head_dim) {
         case 64: return a.wide ? launch_d<64, true>(a, num_sms, s) : launch_d<64>(a, num_sms, s);
         case 80: return launch_d<80>(a, num_sms, s);

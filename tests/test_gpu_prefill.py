@@ -45,6 +45,17 @@ SWEEP = [
     (2, 130, 1100, 4, 4, 64, False, 0, False, "bf16"),
     (1, 3000, 3000, 4, 2, 64, True, 1100, True, "bf16"),
     (2, 300, 2048, 4, 1, 64, True, 0, False, "bf16"),
+    # head_dim 512 on CTA pairs (even GQA group): two heads per pair, ragged last tiles,
+    # a window, no mask, a chunk after cached keys, more items than the GPU has pairs
+    (2, 300, 300, 8, 2, 512, True, 0, False, "bf16"),
+    (1, 257, 257, 16, 2, 512, True, 0, True, "bf16"),
+    (1, 700, 700, 4, 2, 512, True, 200, False, "bf16"),
+    (1, 200, 200, 2, 1, 512, False, 0, False, "bf16"),
+    (1, 100, 600, 4, 2, 512, True, 0, False, "bf16"),
+    (4, 1024, 1024, 8, 2, 512, True, 0, False, "bf16"),
+    # head_dim 512 with an odd GQA group: the single-CTA form
+    (1, 150, 150, 3, 1, 512, True, 0, False, "bf16"),
+    (1, 200, 200, 5, 5, 512, True, 64, False, "bf16"),
     # fp32 (exact CUDA-core path)
     (1, 64, 64, 4, 2, 64, True, 0, False, "f32"),
     (2, 100, 100, 6, 2, 80, True, 7, False, "f32"),
@@ -112,7 +123,7 @@ def test_gemma4_prefill_sampled_rows(name):
     inp = _workload_inputs(wl)
     out, lse = run_prefill(inp, causal=wl.causal, window=wl.window, scale=wl.scale)
     extra = [64, 128, 256, 1023, 1024, 2048, 4096]
-    rows = W.sample_rows(wl.B * wl.S, wl.S, extra=extra, n_random=192)
+    rows = W.sample_rows(wl.B * wl.S, wl.S, extra=extra, n_random=256)
     ref, ref_lse = oracle_prefill(inp, causal=wl.causal, window=wl.window, scale=wl.scale,
                                   rows=rows)
     idx = torch.tensor(rows, device="cuda")
@@ -134,7 +145,7 @@ def test_prefill_long_sequence_sampled_rows(case):
                            seed=W.BASE_SEED + S + D)
     scale = 1.0 / math.sqrt(D)
     out, lse = run_prefill(inp, causal=True, window=window, scale=scale)
-    rows = W.sample_rows(B * S, S, extra=[127, 128, 4095, 4096, S // 2], n_random=64)
+    rows = W.sample_rows(B * S, S, extra=[127, 128, 4095, 4096, S // 2], n_random=256)
     ref, ref_lse = oracle_prefill(inp, causal=True, window=window, scale=scale, rows=rows)
     idx = torch.tensor(rows, device="cuda")
     compare(out.reshape(B * S, Hq, D)[idx], ref, "bf16", str(case),
