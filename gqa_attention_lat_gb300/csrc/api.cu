@@ -74,6 +74,27 @@ bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int heads, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-D bf16 map over the same tensor as make_cache_map, with the head dimension split into
+// 64-column chunks: (d in chunk, row < rows, chunk, head, batch), 128-byte swizzle, box
+// [64, box_rows, box_chunks, 1, 1].  One box lands as box_chunks consecutive
+// [box_rows x 128 B] chunks: a whole multi-chunk tile in one copy.
+bool make_chunked_map(CUtensorMap *m, const void *base, int head_dim, int heads, int rows,
+                      int batch, int64_t row_stride, int64_t head_stride, int64_t seq_stride,
+                      int box_rows, int box_chunks) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr || head_dim % 64 != 0) return false;
+    const cuuint64_t dims[5] = {64, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64),
+                                (cuuint64_t)heads, (cuuint64_t)batch};
+    const cuuint64_t strides[4] = {(cuuint64_t)row_stride * 2, 128, (cuuint64_t)head_stride * 2,
+                                   (cuuint64_t)seq_stride * 2};
+    const cuuint32_t box[5] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 map over decode queries: (head-dim d, query head, sequence), 8-head boxes
 bool make_query_map(CUtensorMap *m, const void *base, int head_dim, int heads, int batch,
                     int64_t row_stride) {
@@ -169,8 +190,18 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
     const int k_box = lat::prefill_tc_box_rows(head_dim, a.wide != 0, a.pair != 0, false);
     const int v_box = lat::prefill_tc_box_rows(head_dim, a.wide != 0, a.pair != 0, true);
     // K/V maps span exactly kv_len rows per sequence: rows past it read as zeros, so cache
-    // slots beyond the visible keys (which may hold anything) never reach the MMA
-    if (!make_head_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, 128) ||
+    // slots beyond the visible keys (which may hold anything) never reach the MMA.  The
+    // pair form moves each tile in one copy (chunked maps: Q 8 chunks of 128 rows, K 8
+    // chunks of its 64 rows, V 2 chunks of 128 rows).
+    if (a.pair) {
+        if (!make_chunked_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, head_dim,
+                              (int64_t)seq_len * q_rs, 128, head_dim / 64) ||
+            !make_chunked_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, kv.k_row,
+                              kv.k_head, kv.k_seq, k_box, head_dim / 64) ||
+            !make_chunked_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, kv.v_row,
+                              kv.v_head, kv.v_seq, v_box, 2))
+            return LAT_ERR_CUDA;
+    } else if (!make_head_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, 128) ||
         !make_cache_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, kv.k_row, kv.k_head,
                         kv.k_seq, k_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
         !make_cache_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, kv.v_row, kv.v_head,

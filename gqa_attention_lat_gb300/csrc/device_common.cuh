@@ -330,6 +330,18 @@ __device__ __forceinline__ void tma_load_4d_pair(void *smem_dst, const void *des
           "r"(c2), "r"(c3)
         : "memory");
 }
+// the same with a 5-D map (d within a 64-column chunk, row, chunk, head, batch): a box of
+// several chunks lands as consecutive [rows x 128 B] chunks, so one copy moves a whole tile
+__device__ __forceinline__ void tma_load_5d_pair(void *smem_dst, const void *desc,
+                                                 uint32_t bar_cluster_addr, int c0, int c1,
+                                                 int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+        ::"r"(smem_u32(smem_dst)), "l"(desc), "r"(bar_cluster_addr), "r"(c0), "r"(c1),
+          "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
 // tensor memory of both CTAs, allocated, released and freed by one warp in each
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *smem_result, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"

@@ -251,8 +251,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
             mbar_init(&bar_s[i], 1);
-            // P: every softmax thread of both CTAs arrives on the even CTA's barrier
-            mbar_init(&bar_p[i], P ? 2 * kSoftmaxThreads : kSoftmaxThreads);
+            // one arrival per softmax warp (of both CTAs on a pair, at the even CTA)
+            mbar_init(&bar_p[i], (P ? 2 : 1) * kSoftmaxThreads / 32);
         }
         for (int q = 0; q < 4; ++q) mbar_init(&bar_x[q], 2);  // one arrival per warp
         mbar_init(bar_o, 1);
@@ -325,14 +325,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(&q_full[qs], arm * C::kQBytes);
-                    for (int c = 0; c < C::kQkChunks; ++c) {
-                        unsigned char *dst = sQ + qs * C::kQBytes + c * kBM * 128;
-                        if constexpr (P)
-                            tma_load_4d_pair(dst, &a.tm_q, cluster_addr(&q_full[qs], 0),
-                                             c * kChunkCols, it.h, it.m0, it.b);
-                        else
-                            tma_load_4d(dst, &a.tm_q, &q_full[qs], c * kChunkCols, it.h, it.m0,
-                                        it.b);
+                    if constexpr (P) {  // the whole query tile in one copy
+                        tma_load_5d_pair(sQ + qs * C::kQBytes, &a.tm_q,
+                                         cluster_addr(&q_full[qs], 0), 0, it.m0, 0, it.h, it.b);
+                    } else {
+                        for (int c = 0; c < C::kQkChunks; ++c)
+                            tma_load_4d(sQ + qs * C::kQBytes + c * kBM * 128, &a.tm_q,
+                                        &q_full[qs], c * kChunkCols, it.h, it.m0, it.b);
                     }
                     ++qi;
                 }
@@ -348,14 +347,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     }
                     if (is_k && a.test_skip_kv_load && g == 0) continue;  // test hook: never load
                     if (leader) mbar_arrive_expect_tx(&full[s], arm * tile_bytes);
-                    for (int c = 0; c < chunks; ++c) {
-                        unsigned char *dst = ring + s * tile_bytes + c * chunk_bytes;
-                        if constexpr (P)
-                            tma_load_4d_pair(dst, tm, cluster_addr(&full[s], 0),
-                                             col0 + c * kChunkCols, it.hk, t * BN + row_off, it.b);
-                        else
-                            tma_load_4d(dst, tm, &full[s], col0 + c * kChunkCols, it.hk,
-                                        t * BN + row_off, it.b);
+                    if constexpr (P) {  // this CTA's part of the tile in one copy
+                        tma_load_5d_pair(ring + s * tile_bytes, tm, cluster_addr(&full[s], 0), 0,
+                                         t * BN + row_off, col0 / kChunkCols, it.hk, it.b);
+                    } else {
+                        for (int c = 0; c < chunks; ++c)
+                            tma_load_4d(ring + s * tile_bytes + c * chunk_bytes, tm, &full[s],
+                                        col0 + c * kChunkCols, it.hk, t * BN + row_off, it.b);
                     }
                 }
             }
@@ -516,11 +514,12 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             const bool r = wait_bar(bar, parity);
             return __all_sync(0xffffffffu, r) != 0;
         };
-        // publish v for the partner warp and read the partner's value
+        // publish v for the partner warp and read the partner's value (the warp barrier
+        // orders every lane's store before lane 0's arrival, whose release makes them
+        // visible to the partner warp's acquire)
         auto exchange = [&](float v, float &other) {
             const int n = xn++;
             xchg[((n & 1) * 2 + wg) * kBM + row] = v;
-            __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_x[quarter]);
             if (!wait_warp(&bar_x[quarter], n & 1)) return false;
@@ -638,11 +637,16 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                 tc_wait_st();
                 l_part = l_part * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
                 m_ref = m_new;
+                // P(g) is published once per warp: every lane's tensor-memory stores are
+                // complete (wait::st) and fenced before the warp barrier, then lane 0 arrives
                 tc_fence_before();
-                if constexpr (P)
-                    mbar_arrive_cluster(bar_p_pair[gt & 1]);
-                else
-                    mbar_arrive(&bar_p[gt & 1]);
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (P)
+                        mbar_arrive_cluster(bar_p_pair[gt & 1]);
+                    else
+                        mbar_arrive(&bar_p[gt & 1]);
+                }
             }
             if (!ok) break;
             g += n_tiles;
