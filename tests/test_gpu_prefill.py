@@ -53,6 +53,9 @@ SWEEP = [
     (1, 200, 200, 2, 1, 512, False, 0, False, "bf16"),
     (1, 100, 600, 4, 2, 512, True, 0, False, "bf16"),
     (4, 1024, 1024, 8, 2, 512, True, 0, False, "bf16"),
+    # head_dim 256 with an odd GQA group: the single-CTA form (even groups run on pairs)
+    (1, 300, 300, 3, 1, 256, True, 0, False, "bf16"),
+    (2, 260, 400, 6, 2, 256, True, 100, False, "bf16"),
     # head_dim 512 with an odd GQA group: the single-CTA form
     (1, 150, 150, 3, 1, 512, True, 0, False, "bf16"),
     (1, 200, 200, 5, 5, 512, True, 64, False, "bf16"),
