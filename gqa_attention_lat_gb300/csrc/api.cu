@@ -424,6 +424,8 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
     a.counters = reinterpret_cast<int32_t *>(ws + plan.part_o_bytes + plan.part_lse_bytes);
     a.max_splits = plan.max_splits;
     a.min_seg = plan.min_seg;
+    a.defer_merge = plan.defer_merge;
+    a.piece_count = a.counters;  // the same scratch region, used one way or the other
     a.status = status;
     return lat::launch_decode_bf16(a, plan.grid, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
 }

@@ -172,6 +172,9 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
         const SeqKeys sk = seq_keys_of(a, kv_len);
         my_sum += (long long)seq_tiles<T>(sk) * HU;
         if (blockIdx.x == 0) {  // CTA 0 handles sequences with nothing to stream
+            if (a.defer_merge && (kv_len < 0 || kv_len > a.max_kv_len || sk.n == 0))
+                for (int h = 0; h < a.n_heads; ++h)  // the merge kernel leaves them alone
+                    a.piece_count[(int64_t)b * a.n_heads + h] = 0;
             if (kv_len < 0 || kv_len > a.max_kv_len) {
                 report_status(a.status, kErrBounds);
             } else if (sk.n == 0) {
@@ -538,6 +541,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] *= rl;
                 const float lse2 = mu + log2f(l);  // log2 domain
+                if (a.defer_merge && x == 0 && r.slot == 0)
+                    a.piece_count[(int64_t)r.b * a.n_heads + h_base + g] = r.nseg;
                 if (single) {
                     *reinterpret_cast<uint4 *>(a.out + (int64_t)r.b * a.out_rs +
                                                (int64_t)(h_base + g) * D + x) =
@@ -553,7 +558,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
-            if (!single) {
+            if (!single && !a.defer_merge) {
                 // Ticket: the warp that brings the unit's count to nseg * kWarps is the last
                 // writer of its partials and queues the unit for merging after the stream.
                 // The result is only examined after the stream, so the round trip overlaps it.
@@ -698,6 +703,72 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     }
 }
 
+// The deferred split-KV merge for few long units: one CTA per (sequence, query head)
+// combines that head's pieces, lse_c and normalised o_c, as
+//   lse = log2 sum_c 2^{lse_c} (log2 domain),  out = sum_c 2^{lse_c - lse} o_c,
+// its 8 warps taking every 8th piece (all of a piece row's columns at once, as 16-byte
+// loads) and meeting in shared memory.
+constexpr int kMergeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a) {
+    __shared__ __align__(16) float red[kMergeThreads / 32][D];
+    const int bh = blockIdx.x;
+    const int nseg = a.piece_count[bh];
+    if (nseg <= 1) return;  // written whole by its only piece (or nothing to write)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *pl = a.part_lse + (int64_t)bh * a.max_splits;
+    const float *po = a.part_o + (int64_t)bh * a.max_splits * D;
+    float M = -INFINITY;
+    for (int sp = lane; sp < nseg; sp += 32) M = fmaxf(M, __ldcg(pl + sp));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    constexpr int kV4 = D / 4;                    // 16-byte vectors per piece row
+    constexpr int kPerLane = (kV4 + 31) / 32;
+    float4 acc[kPerLane];
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Z = 0.f;  // this warp's share of the weight sum
+#pragma unroll 4
+    for (int sp = warp; sp < nseg; sp += kMergeThreads / 32) {
+        const float l = __ldcg(pl + sp);
+        const float w = l == -INFINITY ? 0.f : fast_exp2(l - M);
+        Z += w;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+            const int x4 = lane + 32 * k;
+            if (x4 < kV4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)sp * D) + x4);
+                acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) {
+        const int x4 = lane + 32 * k;
+        if (x4 < kV4) reinterpret_cast<float4 *>(red[warp])[x4] = acc[k];
+    }
+    __shared__ float zs[kMergeThreads / 32];
+    if (lane == 0) zs[warp] = Z;
+    __syncthreads();
+    float zt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) zt += zs[w];
+    const float rz = 1.f / zt;
+    const int b = bh / a.n_heads, h = bh % a.n_heads;
+    for (int x = threadIdx.x; x < D / 2; x += kMergeThreads) {
+        float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeThreads / 32; ++w) {
+            o0 += red[w][2 * x];
+            o1 += red[w][2 * x + 1];
+        }
+        *reinterpret_cast<uint32_t *>(a.out + (int64_t)b * a.out_rs + (int64_t)h * D + 2 * x) =
+            pack_bf16x2(o0 * rz, o1 * rz);
+    }
+    if (threadIdx.x == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(zt)) * kLn2;
+}
+
 template <int D>
 cudaError_t launch_decode_d(const DecodeArgs &a, int grid, cudaStream_t s) {
     using C = DecodeCfg<D>;
@@ -705,6 +776,8 @@ cudaError_t launch_decode_d(const DecodeArgs &a, int grid, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     decode_bf16_kernel<D><<<grid, C::kThreads, C::kSmem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess || !a.defer_merge) return e;
+    decode_merge_kernel<D><<<a.batch * a.n_heads, kMergeThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -737,7 +810,9 @@ int decode_bf16_tile_keys(int head_dim) {
 
 // Pieces are at least min_seg keys long, so a unit of at most `range` keys falls into at
 // most range / min_seg + 2 pieces; min_seg grows with the range so that the count stays
-// near 64 (the scratch layout is sized for it).
+// near 64 (the scratch layout is sized for it).  Shapes with few units, where that would
+// leave CTAs idle, take the deferred-merge plan below instead.
+constexpr int64_t kDeferPieces = 16;
 static int min_seg_for(int range, int T) {
     const int m = std::max(4 * T, (range + 63) / 64);
     return (m + T - 1) / T * T;
@@ -763,18 +838,29 @@ bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int 
     const int G = n_heads / n_kv_heads;
     const int HB = (G + kHeadsPerBlock - 1) / kHeadsPerBlock;
     const int64_t units = (int64_t)batch * n_kv_heads * HB;
+    const int grid = num_sms * occ;
     // the scratch layout uses the window-free bound, so one workspace fits every window
     const int layout_range = std::max(max_kv_len, 1);
-    const int min_seg = min_seg_for(layout_range, T);
+    // pieces per unit that would keep every CTA streaming; when that is more than the
+    // in-kernel merge stages well, cut the stream that finely and merge in a second kernel
+    const int64_t target = (grid + units - 1) / units;
+    const bool defer = target > kDeferPieces;
+    int min_seg = min_seg_for(layout_range, T);
+    if (defer) {
+        const int64_t m = std::max<int64_t>(4 * T, (layout_range + target - 1) / target);
+        min_seg = (int)((m + T - 1) / T * T);
+    }
     const int layout_splits = (layout_range + min_seg - 1) / min_seg + 2;
     p->head_blocks = HB;
     p->min_seg = min_seg;
     p->max_splits = layout_splits;
-    p->grid = num_sms * occ;
+    p->grid = grid;
+    p->defer_merge = defer ? 1 : 0;
     auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
     p->part_o_bytes = round256((size_t)batch * n_heads * layout_splits * head_dim * 4);
     p->part_lse_bytes = round256((size_t)batch * n_heads * layout_splits * 4);
-    p->counter_bytes = round256((size_t)units * 4);
+    // merge counters per unit, or (deferred merge) piece counts per (sequence, head)
+    p->counter_bytes = round256((size_t)(defer ? (int64_t)batch * n_heads : units) * 4);
     p->total_bytes = p->part_o_bytes + p->part_lse_bytes + p->counter_bytes;
     (void)window;
     return true;

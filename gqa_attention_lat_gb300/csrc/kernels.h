@@ -87,10 +87,14 @@ struct DecodeArgs {
     int32_t *counters;  // [batch, n_kv_heads, head_blocks]
     int max_splits;  // partial slots per (sequence, KV head, head block)
     int min_seg;     // shortest stretch of one unit's keys a CTA takes (multiple of the tile)
+    // few long units: the key stream is cut across every CTA and the pieces are merged by
+    // a second kernel; piece_count[b, h] (in the counters' place) tells it how many
+    int defer_merge;
+    int32_t *piece_count;  // [batch, n_heads] when defer_merge
     int32_t *status;
 };
 struct DecodePlan {
-    int head_blocks, max_splits, min_seg, grid;
+    int head_blocks, max_splits, min_seg, grid, defer_merge;
     size_t part_o_bytes, part_lse_bytes, counter_bytes, total_bytes;
 };
 // Chooses the split size and the scratch layout; false when the shape is not built.

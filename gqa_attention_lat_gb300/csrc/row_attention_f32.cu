@@ -3,11 +3,12 @@
 //
 // The arithmetic is the row-wise online softmax of the lattice-inference DESIGN page
 // ("Current Design": fused attention, online softmax in registers): keys are visited in
-// order, each score s = scale * q.k is reduced across the warp (then capped as
-// softcap * tanh(s / softcap) when a cap is set: the larql page, "BLAS-Fused Attention",
-// step 2), and the running maximum
-// m, normaliser l and output accumulator o are updated as
-//   m' = max(m, s),  l' = l*e^(m-m') + e^(s-m'),  o' = o*e^(m-m') + e^(s-m')*v.
+// order, a few at a time; each score s = scale * q.k is reduced across the warp (then
+// capped as softcap * tanh(s / softcap) when a cap is set: the larql page, "BLAS-Fused
+// Attention", step 2), and for a block of scores s_u the running maximum m, normaliser l
+// and output accumulator o are updated as
+//   m' = max(m, max_u s_u),  l' = l*e^(m-m') + sum_u e^(s_u-m'),
+//   o' = o*e^(m-m') + sum_u e^(s_u-m')*v_u.
 // fp32 inputs keep fp32 products (no tf32), so the result stays within ~1e-6 of fp64.
 // Lane `lane` owns head dimensions d = lane + 32*t, t < NT.
 #include <math.h>
@@ -51,29 +52,58 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
     }
     const float *kb = a.k + (int64_t)b * a.k_seq + (int64_t)hk * a.k_head;
     const float *vb = a.v + (int64_t)b * a.v_seq + (int64_t)hk * a.v_head;
+    // Keys are taken KB at a time: the block's K and V rows are loaded together, so the
+    // warp waits for one memory round trip per block instead of one per key; the scores
+    // of the block then enter the running maximum and sums together.
+    constexpr int KB = NT <= 2 ? 8 : (NT <= 4 ? 4 : (NT <= 8 ? 2 : 1));
     float m = -INFINITY, l = 0.f;
-    for (int j = lo; j < hi; ++j) {
-        const int64_t jr = a.ring > 0 ? j % a.ring : j;  // ring cache slot
-        const float *kr = kb + jr * a.k_row;
-        float part = 0.f;
+    for (int j0 = lo; j0 < hi; j0 += KB) {
+        float kx[KB][NT], vx[KB][NT];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const int d = lane + 32 * t;
-            if (d < D) part = fmaf(qv[t], kr[d], part);
+        for (int u = 0; u < KB; ++u) {
+            const int j = j0 + u;
+            const bool live = j < hi;
+            const int64_t jr = a.ring > 0 ? j % a.ring : j;  // ring cache slot
+            const float *kr = kb + jr * a.k_row;
+            const float *vr = vb + jr * a.v_row;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const int d = lane + 32 * t;
+                kx[u][t] = (live && d < D) ? kr[d] : 0.f;
+                vx[u][t] = (live && d < D) ? vr[d] : 0.f;
+            }
+        }
+        float sc[KB];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            float part = 0.f;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) part = fmaf(qv[t], kx[u][t], part);
+            sc[u] = part;
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        float s = part * a.scale;
-        if (a.softcap > 0.f) s = a.softcap * tanhf(s / a.softcap);  // Gemma 2 score cap
-        const float m_new = fmaxf(m, s);
-        const float corr = expf(m - m_new);
-        const float w = expf(s - m_new);
-        l = l * corr + w;
-        const float *vr = vb + jr * a.v_row;
+        for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const int d = lane + 32 * t;
-            if (d < D) o[t] = o[t] * corr + w * vr[d];
+            for (int u = 0; u < KB; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
+        float mb = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            float x = sc[u] * a.scale;
+            if (a.softcap > 0.f) x = a.softcap * tanhf(x / a.softcap);  // Gemma 2 score cap
+            sc[u] = j0 + u < hi ? x : -INFINITY;
+            mb = fmaxf(mb, sc[u]);
+        }
+        const float m_new = fmaxf(m, mb);  // finite: key j0 is always visible
+        const float corr = expf(m - m_new);
+        l *= corr;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) o[t] *= corr;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            const float w = expf(sc[u] - m_new);  // 0 for keys past the end
+            l += w;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) o[t] = fmaf(w, vx[u][t], o[t]);
         }
         m = m_new;
     }

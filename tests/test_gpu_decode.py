@@ -29,10 +29,19 @@ SWEEP = [
     (2, 16, 1, 128, 300, [300, 77], 0, "bf16"),           # G = 16: two head blocks
     (3, 4, 2, 512, 2000, [2000, 1500, 1], 0, "bf16"),
     (2, 8, 8, 64, 64, [64, 5], 0, "bf16"),                # G = 1
-    # one long sequence cut into many pieces: about 20 (merged from a shared-memory copy
-    # of the partials) and about 64 (too many to stage: merged straight from L2)
+    # one long sequence among 19 one-token ones (enough units for the in-kernel merge),
+    # cut into many pieces: about 20 (merged from a shared-memory copy of the partials)
+    # and about 60 (too many to stage: merged straight from L2)
+    (20, 8, 1, 128, 5000, [5000] + [1] * 19, 0, "bf16"),
+    (20, 8, 1, 512, 32768, [32768] + [1] * 19, 0, "bf16"),
+    # few units, long keys: the stream is cut across every CTA and a second kernel merges
+    # the pieces (an empty sequence among them, head_dim 80, a window, G = 16)
     (1, 8, 1, 128, 5000, [5000], 0, "bf16"),
     (1, 8, 1, 512, 32768, [32768], 0, "bf16"),
+    (3, 8, 1, 80, 9000, [9000, 0, 4500], 0, "bf16"),
+    (2, 8, 1, 64, 40000, [40000, 3], 0, "bf16"),
+    (1, 8, 1, 256, 20000, [20000], 700, "bf16"),
+    (1, 16, 1, 128, 6000, [6000], 0, "bf16"),
     # sliding window: the visible keys start at a non-zero cache offset
     (4, 8, 2, 128, 3000, [3000, 1024, 1025, 40], 1024, "bf16"),
     (2, 8, 4, 256, 500, [500, 18], 17, "bf16"),
@@ -71,15 +80,20 @@ def test_decode_head_major_cache():
     compare(out.view(B, Hq, D), ref, "bf16", "head-major", lse, ref_lse)
 
 
-def test_decode_workspace_reuse_gives_identical_results():
-    di = W.decode_inputs(6, 16, 2, 128, 2048, kv_lens=None, device="cuda")
-    run = DecodeRun("bf16", 6, 16, 2, 128, 2048)
+@pytest.mark.parametrize("B,Hkv", [(6, 2), (32, 8)], ids=["few-units", "many-units"])
+def test_decode_workspace_reuse_gives_identical_results(B, Hkv):
+    """Calls that reuse a workspace give identical results.  With few units (12 here) the
+    stream is cut across every CTA and merged by a second kernel; with many (256) the
+    in-kernel merge counters must be back at zero after every call."""
+    di = W.decode_inputs(B, 16, Hkv, 128, 2048, kv_lens=None, device="cuda")
+    run = DecodeRun("bf16", B, 16, Hkv, 128, 2048)
     a, la = run_decode(di, window=0, scale=0.08, runner=run)
     b, lb = run_decode(di, window=0, scale=0.08, runner=run)
     assert torch.equal(a, b) and torch.equal(la, lb)
-    # the merge counters are back at zero after every call
-    cnt_off = run.nbytes - 256
-    assert run.ws[cnt_off:].eq(0).all()
+    if Hkv == 8:
+        units = B * Hkv  # one head block per KV head (16 / 8 = 2 query heads each)
+        cnt_off = run.nbytes - (units * 4 + 255) // 256 * 256
+        assert run.ws[cnt_off:].eq(0).all()
 
 
 def test_decode_empty_sequence():
@@ -111,7 +125,8 @@ def test_decode_workspace_too_small():
     assert e.value.status == binding.LAT_ERR_WORKSPACE
 
 
-@pytest.mark.parametrize("name", ["decode_b32_h32_kv8_d128", "gemma4_global_decode"])
+@pytest.mark.parametrize("name", ["decode_b32_h32_kv8_d128", "gemma4_global_decode",
+                                  "decode_b1_kv2_d128_128k"])
 def test_decode_workloads_full(name):
     wl = W.WORKLOADS[name]
     di = W.decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.L, kv_lens=wl.kv_lens, dtype=wl.dtype,
