@@ -234,6 +234,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     fence_proxy_async_smem();  // the scan's generic writes precede the ring's first copies
     __syncthreads();
     const uint64_t deadline = globaltimer_ns() + kTimeoutNs;
+    // a deferred merge kernel may be set up now; it waits for this grid before reading
+    if (a.defer_merge) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == C::kWarps) {
         // ------------------------------------------------------------ producer
@@ -713,6 +715,9 @@ constexpr int kMergeThreads = 256;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a) {
     __shared__ __align__(16) float red[kMergeThreads / 32][D];
+    // launched as a programmatic dependent of the stream: wait until that grid has
+    // finished and its partial results are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int bh = blockIdx.x;
     const int nseg = a.piece_count[bh];
     if (nseg <= 1) return;  // written whole by its only piece (or nothing to write)
@@ -777,7 +782,17 @@ cudaError_t launch_decode_d(const DecodeArgs &a, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     decode_bf16_kernel<D><<<grid, C::kThreads, C::kSmem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess || !a.defer_merge) return e;
-    decode_merge_kernel<D><<<a.batch * a.n_heads, kMergeThreads, 0, s>>>(a);
+    // programmatic dependent launch: the merge grid is set up while the stream runs
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(a.batch * a.n_heads);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a)) != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
