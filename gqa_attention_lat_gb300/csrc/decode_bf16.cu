@@ -827,7 +827,7 @@ int decode_bf16_tile_keys(int head_dim) {
 // most range / min_seg + 2 pieces; min_seg grows with the range so that the count stays
 // near 64 (the scratch layout is sized for it).  Shapes with few units, where that would
 // leave CTAs idle, take the deferred-merge plan below instead.
-constexpr int64_t kDeferPieces = 16;
+constexpr int64_t kDeferPieces = 8;
 static int min_seg_for(int range, int T) {
     const int m = std::max(4 * T, (range + 63) / 64);
     return (m + T - 1) / T * T;
@@ -856,8 +856,9 @@ bool plan_decode_bf16(int batch, int n_heads, int n_kv_heads, int head_dim, int 
     const int grid = num_sms * occ;
     // the scratch layout uses the window-free bound, so one workspace fits every window
     const int layout_range = std::max(max_kv_len, 1);
-    // pieces per unit that would keep every CTA streaming; when that is more than the
-    // in-kernel merge stages well, cut the stream that finely and merge in a second kernel
+    // pieces per unit that would keep every CTA streaming; beyond a few, the last CTA of a
+    // unit would merge many pieces after its stream (about 8 us at head_dim 512, measured),
+    // so cut the stream that finely and merge in a second kernel
     const int64_t target = (grid + units - 1) / units;
     const bool defer = target > kDeferPieces;
     int min_seg = min_seg_for(layout_range, T);

@@ -29,11 +29,11 @@ SWEEP = [
     (2, 16, 1, 128, 300, [300, 77], 0, "bf16"),           # G = 16: two head blocks
     (3, 4, 2, 512, 2000, [2000, 1500, 1], 0, "bf16"),
     (2, 8, 8, 64, 64, [64, 5], 0, "bf16"),                # G = 1
-    # one long sequence among 19 one-token ones (enough units for the in-kernel merge),
+    # one long sequence among 39 one-token ones (enough units for the in-kernel merge),
     # cut into many pieces: about 20 (merged from a shared-memory copy of the partials)
     # and about 60 (too many to stage: merged straight from L2)
-    (20, 8, 1, 128, 5000, [5000] + [1] * 19, 0, "bf16"),
-    (20, 8, 1, 512, 32768, [32768] + [1] * 19, 0, "bf16"),
+    (40, 8, 1, 128, 5000, [5000] + [1] * 39, 0, "bf16"),
+    (40, 8, 1, 512, 32768, [32768] + [1] * 39, 0, "bf16"),
     # few units, long keys: the stream is cut across every CTA and a second kernel merges
     # the pieces (an empty sequence among them, head_dim 80, a window, G = 16)
     (1, 8, 1, 128, 5000, [5000], 0, "bf16"),
