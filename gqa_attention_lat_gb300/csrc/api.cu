@@ -190,16 +190,18 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
     const int k_box = lat::prefill_tc_box_rows(head_dim, a.wide != 0, a.pair != 0, false);
     const int v_box = lat::prefill_tc_box_rows(head_dim, a.wide != 0, a.pair != 0, true);
     // K/V maps span exactly kv_len rows per sequence: rows past it read as zeros, so cache
-    // slots beyond the visible keys (which may hold anything) never reach the MMA.  The
-    // pair form moves each tile in one copy (chunked maps: Q 8 chunks of 128 rows, K 8
-    // chunks of its 64 rows, V 2 chunks of 128 rows).
-    if (a.pair) {
+    // slots beyond the visible keys (which may hold anything) never reach the MMA.  Head
+    // dims that are whole 64-column chunks move each tile in one copy (chunked maps: Q all
+    // chunks of 128 rows, K all chunks of its rows, V the chunks of this CTA's columns).
+    a.chunked = lat::prefill_tc_chunked(head_dim, a.pair != 0) ? 1 : 0;
+    if (a.chunked) {
+        const int v_chunks = lat::prefill_tc_v_chunks(head_dim, a.pair != 0);
         if (!make_chunked_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, head_dim,
                               (int64_t)seq_len * q_rs, 128, head_dim / 64) ||
             !make_chunked_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, kv.k_row,
                               kv.k_head, kv.k_seq, k_box, head_dim / 64) ||
             !make_chunked_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, kv.v_row,
-                              kv.v_head, kv.v_seq, v_box, 2))
+                              kv.v_head, kv.v_seq, v_box, v_chunks))
             return LAT_ERR_CUDA;
     } else if (!make_head_map(&a.tm_q, q, head_dim, n_heads, seq_len, batch, q_rs, 128) ||
         !make_cache_map(&a.tm_k, k, head_dim, n_kv_heads, kv_len, batch, kv.k_row, kv.k_head,

@@ -106,6 +106,18 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *desc, ui
         : "memory");
 }
 
+// 5-D tile (a chunked map: d within a 64-column chunk, row, chunk, head, batch), one copy
+// landing several [rows x 128 B] chunks back to back
+__device__ __forceinline__ void tma_load_5d(void *smem_dst, const void *desc, uint64_t *bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+        ::"r"(smem_u32(smem_dst)), "l"(desc), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+          "r"(c3), "r"(c4)
+        : "memory");
+}
+
 // contiguous global -> shared copy of `bytes` (multiple of 16, both ends 16-byte aligned)
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
                                           uint64_t *bar) {

@@ -123,6 +123,7 @@ struct PrefillTcArgs {
     int test_skip_kv_load;         // test hook: never load KV tile 0 (forces a timeout)
     int wide;                      // head_dim 64: the 96-key-tile form (prefill_tc_wide)
     int pair;                      // head_dim 512, even GQA group: the CTA-pair form
+    int chunked;                   // tm_q/k/v are chunked 5-D maps: one copy per tile
 };
 // the 96-key-tile form of head_dim 64 for long key ranges (a query tile visiting ~1K keys)
 bool prefill_tc_wide(int head_dim, int seq_len, int kv_len, int causal, int window);
@@ -131,6 +132,10 @@ int prefill_tc_block_n(int head_dim, bool wide);  // keys per KV tile
 bool prefill_tc_pair(int head_dim, int n_heads, int n_kv_heads);
 // rows of the K (v = false) or V (v = true) tensor-map box of the chosen form
 int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v);
+// forms that move each tile in one copy through chunked 5-D maps, and the 64-column
+// chunks of one V copy
+bool prefill_tc_chunked(int head_dim, bool pair);
+int prefill_tc_v_chunks(int head_dim, bool pair);
 // work items of one prefill launch (query tile x head x output-column part); the kernel
 // numbers them in int32, so the host refuses shapes above kPrefillMaxItems
 int64_t prefill_tc_items(int batch, int n_heads, int head_dim, int seq_len);

@@ -328,6 +328,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     if constexpr (P) {  // the whole query tile in one copy
                         tma_load_5d_pair(sQ + qs * C::kQBytes, &a.tm_q,
                                          cluster_addr(&q_full[qs], 0), 0, it.m0, 0, it.h, it.b);
+                    } else if (a.chunked) {
+                        tma_load_5d(sQ + qs * C::kQBytes, &a.tm_q, &q_full[qs], 0, it.m0, 0,
+                                    it.h, it.b);
                     } else {
                         for (int c = 0; c < C::kQkChunks; ++c)
                             tma_load_4d(sQ + qs * C::kQBytes + c * kBM * 128, &a.tm_q,
@@ -350,6 +353,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     if constexpr (P) {  // this CTA's part of the tile in one copy
                         tma_load_5d_pair(ring + s * tile_bytes, tm, cluster_addr(&full[s], 0), 0,
                                          t * BN + row_off, col0 / kChunkCols, it.hk, it.b);
+                    } else if (a.chunked) {
+                        tma_load_5d(ring + s * tile_bytes, tm, &full[s], 0, t * BN + row_off,
+                                    col0 / kChunkCols, it.hk, it.b);
                     } else {
                         for (int c = 0; c < chunks; ++c)
                             tma_load_4d(ring + s * tile_bytes + c * chunk_bytes, tm, &full[s],
@@ -784,6 +790,20 @@ int prefill_tc_block_n(int head_dim, bool wide) {
 int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v) {
     if (pair) return v ? TcCfg<512, false, true>::kBN : TcCfg<512, false, true>::kKRows;
     return prefill_tc_block_n(head_dim, wide);
+}
+
+bool prefill_tc_chunked(int head_dim, bool pair) {
+    return pair || head_dim == 128 || head_dim == 256 || head_dim == 512;
+}
+
+int prefill_tc_v_chunks(int head_dim, bool pair) {
+    if (pair) return TcCfg<512, false, true>::kVChunks;
+    switch (head_dim) {
+        case 128: return TcCfg<128>::kVChunks;
+        case 256: return TcCfg<256>::kVChunks;
+        case 512: return TcCfg<512>::kVChunks;
+        default: return 0;
+    }
 }
 
 int64_t prefill_tc_items(int batch, int n_heads, int head_dim, int seq_len) {
