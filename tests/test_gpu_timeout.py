@@ -23,8 +23,12 @@ def _lib(cuda_device):
     ensure_library()
 
 
-def test_prefill_wait_times_out_and_context_survives():
-    B, S, Hq, Hkv, D = 1, 256, 4, 2, 128
+@pytest.mark.parametrize("D", [128, 512], ids=["single-CTA", "CTA-pair"])
+def test_prefill_wait_times_out_and_context_survives(D):
+    """head_dim 128 runs one CTA per item; head_dim 512 with two query heads per KV head
+    runs on CTA pairs, where the even CTA waits for the tile and the odd CTA's waits for
+    the S it never gets run out in the same way."""
+    B, S, Hq, Hkv = 1, 256, 4, 2
     inp = W.prefill_inputs(B, S, S, Hq, Hkv, D, dtype="bf16", device="cuda")
     out = torch.zeros((B * S, Hq * D), dtype=torch.bfloat16, device="cuda")
     st = status_tensor()
