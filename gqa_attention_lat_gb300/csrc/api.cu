@@ -80,7 +80,8 @@ bool make_cache_map(CUtensorMap *m, const void *base, int head_dim, int heads, i
 // [box_rows x 128 B] chunks: a whole multi-chunk tile in one copy.
 bool make_chunked_map(CUtensorMap *m, const void *base, int head_dim, int heads, int rows,
                       int batch, int64_t row_stride, int64_t head_stride, int64_t seq_stride,
-                      int box_rows, int box_chunks) {
+                      int box_rows, int box_chunks,
+                      CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (fn == nullptr || head_dim % 64 != 0) return false;
     const cuuint64_t dims[5] = {64, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64),
@@ -90,8 +91,7 @@ bool make_chunked_map(CUtensorMap *m, const void *base, int head_dim, int heads,
     const cuuint32_t box[5] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks, 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -393,11 +393,23 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
     lat::DecodeArgs a{};
     if (max_kv_len > 0) {
         const int box = lat::decode_bf16_tile_keys(head_dim);
-        if (!make_cache_map(&a.tm_k, k_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
-                            cache_head_stride, cache_seq_stride, box) ||
-            !make_cache_map(&a.tm_v, v_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
-                            cache_head_stride, cache_seq_stride, box) ||
-            !make_query_map(&a.tm_q, q, head_dim, n_heads, batch, q_rs))
+        // head dims of up to four whole 64-column chunks take each K (or V) tile in one
+        // copy (at head_dim 512, eight 32-row chunks per copy measured 2.4 % slower than
+        // eight copies)
+        a.chunked = head_dim % 64 == 0 && head_dim <= 256 ? 1 : 0;
+        const bool maps_ok =
+            a.chunked
+                ? make_chunked_map(&a.tm_k, k_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
+                                   cache_head_stride, cache_seq_stride, box, head_dim / 64,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
+                      make_chunked_map(&a.tm_v, v_cache, head_dim, n_kv_heads, rows, batch,
+                                       cache_rs, cache_head_stride, cache_seq_stride, box,
+                                       head_dim / 64, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+                : make_cache_map(&a.tm_k, k_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
+                                 cache_head_stride, cache_seq_stride, box) &&
+                      make_cache_map(&a.tm_v, v_cache, head_dim, n_kv_heads, rows, batch,
+                                     cache_rs, cache_head_stride, cache_seq_stride, box);
+        if (!maps_ok || !make_query_map(&a.tm_q, q, head_dim, n_heads, batch, q_rs))
             return LAT_ERR_CUDA;
     }
     a.q = static_cast<const __nv_bfloat16 *>(q);

@@ -300,9 +300,16 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                         unsigned char *dk = sRing + s * C::kStageBytes;
                         unsigned char *dv = dk + C::kTileBytes;
-                        for (int c = 0; c < C::kCols64; ++c) {
-                            tma_load_4d(dk + c * C::kTile * 128, &a.tm_k, &full[s], c * 64, hk, key0, b);
-                            tma_load_4d(dv + c * C::kTile * 128, &a.tm_v, &full[s], c * 64, hk, key0, b);
+                        if (a.chunked) {  // each tile's 64-column chunks in one copy
+                            tma_load_5d(dk, &a.tm_k, &full[s], 0, key0, 0, hk, b);
+                            tma_load_5d(dv, &a.tm_v, &full[s], 0, key0, 0, hk, b);
+                        } else {
+                            for (int c = 0; c < C::kCols64; ++c) {
+                                tma_load_4d(dk + c * C::kTile * 128, &a.tm_k, &full[s], c * 64,
+                                            hk, key0, b);
+                                tma_load_4d(dv + c * C::kTile * 128, &a.tm_v, &full[s], c * 64,
+                                            hk, key0, b);
+                            }
                         }
                         ++tg;
                     }

@@ -91,6 +91,7 @@ struct DecodeArgs {
     // a second kernel; piece_count[b, h] (in the counters' place) tells it how many
     int defer_merge;
     int32_t *piece_count;  // [batch, n_heads] when defer_merge
+    int chunked;           // tm_k/tm_v are chunked 5-D maps: one copy per K or V tile
     int32_t *status;
 };
 struct DecodePlan {
