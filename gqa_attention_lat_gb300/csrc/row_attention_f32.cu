@@ -1,5 +1,5 @@
-// row_attention_f32.cu — exact-fp32 attention on the CUDA cores, one warp per
-// (query row, query head).  Serves every LAT_F32 call (prefill and decode).
+// row_attention_f32.cu — exact-fp32 attention on the CUDA cores, one CTA of four warps
+// per (query row, query head).  Serves every LAT_F32 call (prefill and decode).
 //
 // The arithmetic is the row-wise online softmax of the lattice-inference DESIGN page
 // ("Current Design": fused attention, online softmax in registers): keys are visited in
@@ -9,6 +9,10 @@
 // and output accumulator o are updated as
 //   m' = max(m, max_u s_u),  l' = l*e^(m-m') + sum_u e^(s_u-m'),
 //   o' = o*e^(m-m') + sum_u e^(s_u-m')*v_u.
+// The four warps take interleaved blocks of the row's keys, each keeping its own (m, l, o),
+// and meet in shared memory at the end, where the states combine as
+//   M = max_w m_w,  l = sum_w l_w e^(m_w - M),  out = sum_w o_w e^(m_w - M) / l,
+// so a row waits for a quarter of the memory round trips one warp would.
 // fp32 inputs keep fp32 products (no tf32), so the result stays within ~1e-6 of fp64.
 // Lane `lane` owns head dimensions d = lane + 32*t, t < NT.
 #include <math.h>
@@ -18,12 +22,14 @@
 
 namespace lat {
 
+constexpr int kRowWarps = 4;
+
 template <int NT>
-__global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t unit = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int64_t n_units = (int64_t)a.batch * a.seq_len * a.n_heads;
-    if (unit >= n_units) return;
+__global__ void __launch_bounds__(32 * kRowWarps) row_attention_f32_kernel(RowAttnArgs a) {
+    __shared__ float part_m[kRowWarps], part_l[kRowWarps];
+    __shared__ float part_o[kRowWarps][32 * NT];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t unit = blockIdx.x;
     const int h = (int)(unit % a.n_heads);
     const int64_t r = unit / a.n_heads;  // flattened query row b*seq_len + i
     const int b = (int)(r / a.seq_len), i = (int)(r % a.seq_len);
@@ -32,8 +38,8 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
     int L = a.kv_len;
     if (a.kv_lens != nullptr) {
         L = a.kv_lens[b];
-        if (L < 0 || L > a.max_kv_len) {
-            if (lane == 0 && h == 0) report_status(a.status, kErrBounds);
+        if (L < 0 || L > a.max_kv_len) {  // the whole CTA leaves
+            if (threadIdx.x == 0 && h == 0) report_status(a.status, kErrBounds);
             return;
         }
     }
@@ -57,7 +63,7 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
     // of the block then enter the running maximum and sums together.
     constexpr int KB = NT <= 2 ? 8 : (NT <= 4 ? 4 : (NT <= 8 ? 2 : 1));
     float m = -INFINITY, l = 0.f;
-    for (int j0 = lo; j0 < hi; j0 += KB) {
+    for (int j0 = lo + warp * KB; j0 < hi; j0 += kRowWarps * KB) {
         float kx[KB][NT], vx[KB][NT];
 #pragma unroll
         for (int u = 0; u < KB; ++u) {
@@ -93,7 +99,7 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
             sc[u] = j0 + u < hi ? x : -INFINITY;
             mb = fmaxf(mb, sc[u]);
         }
-        const float m_new = fmaxf(m, mb);  // finite: key j0 is always visible
+        const float m_new = fmaxf(m, mb);  // finite: key j0 is visible
         const float corr = expf(m - m_new);
         l *= corr;
 #pragma unroll
@@ -107,29 +113,51 @@ __global__ void __launch_bounds__(128) row_attention_f32_kernel(RowAttnArgs a) {
         }
         m = m_new;
     }
-    const bool empty = hi <= lo;
-    const float inv_l = empty ? 0.f : 1.f / l;
+    // the four warps' states meet in shared memory; warp 0 combines and writes the row
+#pragma unroll
+    for (int t = 0; t < NT; ++t) part_o[warp][lane + 32 * t] = o[t];
+    if (lane == 0) {
+        part_m[warp] = m;
+        part_l[warp] = l;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kRowWarps; ++w) M = fmaxf(M, part_m[w]);
+    const bool empty = !(M > -INFINITY);  // no visible key
+    float f[kRowWarps], lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRowWarps; ++w) {
+        f[w] = empty ? 0.f : expf(part_m[w] - M);  // 0 for a warp that saw no key
+        lt += part_l[w] * f[w];
+    }
+    const float inv_l = empty ? 0.f : 1.f / lt;
     float *orow = a.out + r * a.out_rs + (int64_t)h * D;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const int d = lane + 32 * t;
-        if (d < D) orow[d] = o[t] * inv_l;
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kRowWarps; ++w) acc = fmaf(part_o[w][d], f[w], acc);
+        if (d < D) orow[d] = acc * inv_l;
     }
     if (a.lse != nullptr && lane == 0)
-        a.lse[r * a.n_heads + h] = empty ? -INFINITY : m + logf(l);
+        a.lse[r * a.n_heads + h] = empty ? -INFINITY : M + logf(lt);
 }
 
 cudaError_t launch_row_attention_f32(const RowAttnArgs &a, cudaStream_t s) {
     const int64_t n_units = (int64_t)a.batch * a.seq_len * a.n_heads;
     if (n_units == 0) return cudaSuccess;
-    const int64_t blocks = (n_units + 3) / 4;
+    const int64_t blocks = n_units;  // one CTA per (row, head)
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    constexpr int kT = 32 * kRowWarps;
     switch (a.head_dim) {
-        case 64: row_attention_f32_kernel<2><<<(unsigned)blocks, 128, 0, s>>>(a); break;
-        case 80: row_attention_f32_kernel<3><<<(unsigned)blocks, 128, 0, s>>>(a); break;
-        case 128: row_attention_f32_kernel<4><<<(unsigned)blocks, 128, 0, s>>>(a); break;
-        case 256: row_attention_f32_kernel<8><<<(unsigned)blocks, 128, 0, s>>>(a); break;
-        case 512: row_attention_f32_kernel<16><<<(unsigned)blocks, 128, 0, s>>>(a); break;
+        case 64: row_attention_f32_kernel<2><<<(unsigned)blocks, kT, 0, s>>>(a); break;
+        case 80: row_attention_f32_kernel<3><<<(unsigned)blocks, kT, 0, s>>>(a); break;
+        case 128: row_attention_f32_kernel<4><<<(unsigned)blocks, kT, 0, s>>>(a); break;
+        case 256: row_attention_f32_kernel<8><<<(unsigned)blocks, kT, 0, s>>>(a); break;
+        case 512: row_attention_f32_kernel<16><<<(unsigned)blocks, kT, 0, s>>>(a); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
