@@ -887,6 +887,18 @@ def kernel_info(wl, step, peaks):
             "decode_bf16_%s.md" % wl.name, ["decode_bf16.cu", "device_common.cuh", "kernels.h"])
 
 
+def launches_per_step(wl, device):
+    """The library's kernel launches in one timed step: one, plus the deferred split-KV
+    merge for decode shapes whose units are too few to keep every CTA streaming (the
+    plan's rule: more than 8 pieces per unit needed, at the kernel's CTAs per SM)."""
+    if wl.kind != "decode" or wl.dtype != "bf16":
+        return 1
+    ctas_per_sm = {64: 3, 80: 2, 128: 2, 256: 2, 512: 1}[wl.D]
+    grid = torch.cuda.get_device_properties(device).multi_processor_count * ctas_per_sm
+    units = wl.B * wl.Hkv * ((wl.Hq // wl.Hkv + 7) // 8)
+    return 2 if -(-grid // units) > 8 else 1
+
+
 def measure_main(wl, device, flush, stream, peaks, peak_src, args, world, dist):
     """Warm-up, the timed steps (max over ranks), roofline and e2e of one workload."""
     step = {"prefill": PrefillStep, "prefill_cached": PrefillCachedStep,
@@ -926,9 +938,9 @@ def measure_main(wl, device, flush, stream, peaks, peak_src, args, world, dist):
                 "hbm_frac": alg_bytes / (kernel_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
     e2e = {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
-    # our kernels inside the timed region: one per step (the flush is torch's)
+    # our kernels inside the timed region (the flush is torch's)
     return {"value": value, "unit": unit, "ms_per_step": ms_per_step, "roofline": roofline,
-            "e2e": e2e, "gpu_launches": args.steps}
+            "e2e": e2e, "gpu_launches": args.steps * launches_per_step(wl, device)}
 
 
 def main():
