@@ -618,6 +618,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     __threadfence();
     const int n_merges = min(*n_merge, kMaxMerges);
     float *wts = reinterpret_cast<float *>(sQ);  // [g][nseg] weights, then [g] lse
+    int n_staged = 0;  // completed phases of merge_bar: only staged merges use it
     for (int mi = 0; mi < n_merges; ++mi) {
         const int b = merge_unit[4 * mi + 0], h_base = merge_unit[4 * mi + 1];
         const int g_cnt = merge_unit[4 * mi + 2];
@@ -659,10 +660,10 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                 if (lane == 0) wts[kHeadsPerBlock * nseg + g] = M + log2f(Z);
             }
             __syncthreads();
-            const bool got = mbar_wait_bounded(merge_bar, mi & 1, abort_flag, deadline);
+            const bool got = mbar_wait_bounded(merge_bar, n_staged & 1, abort_flag, deadline);
             if (!__syncthreads_and(got)) {  // the copies must land before the CTA may go
                 volatile int no_abort = 0;
-                mbar_wait_bounded(merge_bar, mi & 1, &no_abort, globaltimer_ns() + 100000000ull);
+                mbar_wait_bounded(merge_bar, n_staged & 1, &no_abort, globaltimer_ns() + 100000000ull);
                 if (tid == 0) report_status(a.status, kErrTimeout);
                 return;
             }
@@ -681,6 +682,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                 if (x == 0 && a.lse != nullptr)
                     a.lse[(int64_t)b * a.n_heads + h_base + g] = wts[kHeadsPerBlock * nseg + g] * kLn2;
             }
+            ++n_staged;
             __syncthreads();  // the ring and weights are reused by the next unit
         } else {
             // too many pieces to stage: one thread per 4 outputs, partials straight from L2

@@ -96,6 +96,24 @@ def test_decode_workspace_reuse_gives_identical_results(B, Hkv):
         assert run.ws[cnt_off:].eq(0).all()
 
 
+def test_decode_mixed_staged_and_direct_merges_repeat_identically():
+    """CTAs that merge, after their stream, one unit with too many pieces to stage (read
+    straight from L2) and one staged from a shared-memory copy.  Ten 40000-key sequences
+    cut into ~28 pieces each sit between 3000-key ones cut into ~3, so about 18 CTAs hold
+    pieces of both kinds; whichever merge a CTA queues first, each staged copy must be
+    waited for on its own barrier phase.  Every launch equals the oracle and the others."""
+    lens = [40000, 3000, 1, 1] * 10
+    B, Hq, Hkv, D, cap = 40, 8, 1, 128, 40000
+    di = W.decode_inputs(B, Hq, Hkv, D, cap, kv_lens=lens, device="cuda", seed=W.BASE_SEED + 77)
+    run = DecodeRun("bf16", B, Hq, Hkv, D, cap)
+    first, first_lse = run_decode(di, window=0, scale=0.09, runner=run)
+    for _ in range(9):
+        out, lse = run_decode(di, window=0, scale=0.09, runner=run)
+        assert torch.equal(out, first) and torch.equal(lse, first_lse)
+    ref, ref_lse = oracle_decode(di, window=0, scale=0.09)
+    compare(first, ref, "bf16", "mixed merges", first_lse, ref_lse)
+
+
 def test_decode_empty_sequence():
     """kv_len 0: nothing visible, out = 0 and lse = -inf."""
     di = W.decode_inputs(2, 4, 2, 64, 64, kv_lens=[0, 10], device="cuda")
