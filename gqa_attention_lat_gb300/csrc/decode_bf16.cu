@@ -714,73 +714,90 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     }
 }
 
-// The deferred split-KV merge for few long units: one CTA per (sequence, query head)
-// combines that head's pieces, lse_c and normalised o_c, as
-//   lse = log2 sum_c 2^{lse_c} (log2 domain),  out = sum_c 2^{lse_c - lse} o_c,
-// its 8 warps taking every 8th piece (all of a piece row's columns at once, as 16-byte
-// loads) and meeting in shared memory.
+// The deferred split-KV merge for few long units: the pieces of one (sequence, query
+// head), lse_c and normalised o_c, combine as
+//   lse = log2 sum_c 2^{lse_c} (log2 domain),  out = sum_c 2^{lse_c - lse} o_c.
+// Each head's columns are split over kMergeSplit<D> CTAs of kMergeV4<D> 16-byte vectors;
+// within a CTA thread t takes column vector t % w4 of pieces t / w4, t / w4 + groups, ...
+// It issues the loads of its first kMergeBatch pieces (lse and partial) at once, so the
+// whole merge costs about one round trip to L2; the maximum lse is a block reduction.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 8;  // pieces per thread held in registers
+template <int D>
+constexpr int kMergeV4 = D >= 256 ? 32 : 8;
+template <int D>
+constexpr int kMergeSplit = (D / 4 + kMergeV4<D> - 1) / kMergeV4<D>;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a) {
-    __shared__ __align__(16) float red[kMergeThreads / 32][D];
+    constexpr int kV4 = D / 4;
+    __shared__ float4 red[kMergeThreads];
+    __shared__ float red_m[kMergeThreads / 32], red_z[kMergeThreads];
     // launched as a programmatic dependent of the stream: wait until that grid has
     // finished and its partial results are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x / kMergeSplit<D>, cb = blockIdx.x % kMergeSplit<D>;
     const int nseg = a.piece_count[bh];
     if (nseg <= 1) return;  // written whole by its only piece (or nothing to write)
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int v0 = cb * kMergeV4<D>, w4 = min(kMergeV4<D>, kV4 - v0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int groups = kMergeThreads / w4;  // w4 divides the block (a power of two or 4)
+    const int g = tid / w4, col = v0 + tid % w4;
+    const bool active = g < groups;
     const float *pl = a.part_lse + (int64_t)bh * a.max_splits;
-    const float *po = a.part_o + (int64_t)bh * a.max_splits * D;
-    float M = -INFINITY;
-    for (int sp = lane; sp < nseg; sp += 32) M = fmaxf(M, __ldcg(pl + sp));
+    const float4 *po = reinterpret_cast<const float4 *>(a.part_o + (int64_t)bh * a.max_splits * D) + col;
+    float lv[kMergeBatch];
+    float4 ov[kMergeBatch];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    constexpr int kV4 = D / 4;                    // 16-byte vectors per piece row
-    constexpr int kPerLane = (kV4 + 31) / 32;
-    float4 acc[kPerLane];
-#pragma unroll
-    for (int k = 0; k < kPerLane; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float Z = 0.f;  // this warp's share of the weight sum
-#pragma unroll 4
-    for (int sp = warp; sp < nseg; sp += kMergeThreads / 32) {
-        const float l = __ldcg(pl + sp);
-        const float w = l == -INFINITY ? 0.f : fast_exp2(l - M);
-        Z += w;
-#pragma unroll
-        for (int k = 0; k < kPerLane; ++k) {
-            const int x4 = lane + 32 * k;
-            if (x4 < kV4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)sp * D) + x4);
-                acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
-            }
-        }
+    for (int k = 0; k < kMergeBatch; ++k) {
+        const int sp = g + k * groups;
+        const bool ok = active && sp < nseg;
+        lv[k] = ok ? __ldcg(pl + sp) : -INFINITY;
+        ov[k] = ok ? __ldcg(po + (int64_t)sp * kV4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float m = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kPerLane; ++k) {
-        const int x4 = lane + 32 * k;
-        if (x4 < kV4) reinterpret_cast<float4 *>(red[warp])[x4] = acc[k];
-    }
-    __shared__ float zs[kMergeThreads / 32];
-    if (lane == 0) zs[warp] = Z;
+    for (int k = 0; k < kMergeBatch; ++k) m = fmaxf(m, lv[k]);
+    for (int sp = g + kMergeBatch * groups; active && sp < nseg; sp += groups) m = fmaxf(m, __ldcg(pl + sp));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) red_m[warp] = m;
     __syncthreads();
-    float zt = 0.f;
+    float M = red_m[0];
 #pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) zt += zs[w];
-    const float rz = 1.f / zt;
-    const int b = bh / a.n_heads, h = bh % a.n_heads;
-    for (int x = threadIdx.x; x < D / 2; x += kMergeThreads) {
-        float o0 = 0.f, o1 = 0.f;
+    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red_m[w]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float z = 0.f;
 #pragma unroll
-        for (int w = 0; w < kMergeThreads / 32; ++w) {
-            o0 += red[w][2 * x];
-            o1 += red[w][2 * x + 1];
-        }
-        *reinterpret_cast<uint32_t *>(a.out + (int64_t)b * a.out_rs + (int64_t)h * D + 2 * x) =
-            pack_bf16x2(o0 * rz, o1 * rz);
+    for (int k = 0; k < kMergeBatch; ++k) {
+        const float wt = lv[k] == -INFINITY ? 0.f : fast_exp2(lv[k] - M);
+        z += wt;
+        acc.x += wt * ov[k].x; acc.y += wt * ov[k].y; acc.z += wt * ov[k].z; acc.w += wt * ov[k].w;
     }
-    if (threadIdx.x == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(zt)) * kLn2;
+    for (int sp = g + kMergeBatch * groups; active && sp < nseg; sp += groups) {
+        const float l = __ldcg(pl + sp);
+        const float wt = l == -INFINITY ? 0.f : fast_exp2(l - M);
+        const float4 v = __ldcg(po + (int64_t)sp * kV4);
+        z += wt;
+        acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
+    }
+    red[tid] = acc;
+    red_z[tid] = z;
+    __syncthreads();
+    if (tid < w4) {  // column vector v0 + tid: sum over the piece groups
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        float zt = 0.f;
+        for (int gg = 0; gg < groups; ++gg) {
+            const float4 v = red[gg * w4 + tid];
+            o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
+            zt += red_z[gg * w4];  // every column's threads saw the same weights
+        }
+        const float rz = 1.f / zt;
+        const int b = bh / a.n_heads, h = bh % a.n_heads;
+        *reinterpret_cast<uint2 *>(a.out + (int64_t)b * a.out_rs + (int64_t)h * D + 4 * (v0 + tid)) =
+            make_uint2(pack_bf16x2(o.x * rz, o.y * rz), pack_bf16x2(o.z * rz, o.w * rz));
+        if (cb == 0 && tid == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(zt)) * kLn2;
+    }
 }
 
 template <int D>
@@ -796,7 +813,7 @@ cudaError_t launch_decode_d(const DecodeArgs &a, int grid, cudaStream_t s) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(a.batch * a.n_heads);
+    cfg.gridDim = dim3(a.batch * a.n_heads * kMergeSplit<D>);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.stream = s;
     cfg.attrs = attr;
