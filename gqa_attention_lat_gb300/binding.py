@@ -64,6 +64,8 @@ _SIGNATURES = {
                              _I32, _I32, _I32, _P, _P]),
     "lat_test_prefill_timeout": (_I32, [_P, _I64, _P, _I64, _P, _I64, _P, _I64, _I32, _I32,
                                         _I32, _I32, _I32, _U64, _P, _P]),
+    "lat_test_decode_timeout": (_I32, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _I64,
+                                       _I32, _I32, _I32, _I32, _P, _SZ, _U64, _P, _P]),
 }
 
 
@@ -224,3 +226,14 @@ def lat_test_prefill_timeout(q, q_rs, k, k_rs, v, v_rs, out, out_rs, batch, seq_
         _ptr(q), q_rs, _ptr(k), k_rs, _ptr(v), v_rs, _ptr(out), out_rs, batch, seq_len,
         n_heads, n_kv_heads, head_dim, timeout_ns, _ptr(status), _stream(stream)),
         "lat_test_prefill_timeout")
+
+
+def lat_test_decode_timeout(q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                            cache_seq_stride, kv_lens, max_kv_len, out, out_rs, batch, n_heads,
+                            n_kv_heads, head_dim, workspace, workspace_bytes, timeout_ns, status,
+                            stream=None):
+    _check(library().lat_test_decode_timeout(
+        _ptr(q), q_rs, _ptr(k_cache), _ptr(v_cache), cache_rs, cache_head_stride,
+        cache_seq_stride, _ptr(kv_lens), max_kv_len, _ptr(out), out_rs, batch, n_heads,
+        n_kv_heads, head_dim, _ptr(workspace), workspace_bytes, timeout_ns, _ptr(status),
+        _stream(stream)), "lat_test_decode_timeout")

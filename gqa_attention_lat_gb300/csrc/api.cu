@@ -325,7 +325,7 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
                        void *out, int64_t out_rs, float *lse, int batch, int n_heads,
                        int n_kv_heads, int head_dim, int window, float scale, float softcap,
                        int ring, void *workspace, size_t workspace_bytes, int32_t *status,
-                       void *stream) {
+                       void *stream, uint64_t timeout_ns, int skip_load) {
     if (dt != LAT_F32 && dt != LAT_BF16) return LAT_ERR_INVALID_ARG;
     if (!(softcap >= 0.f) || !isfinite(softcap)) return LAT_ERR_INVALID_ARG;
     // a ring cache keeps only the last `ring` positions: the window must fit in it
@@ -440,6 +440,8 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
     a.min_seg = plan.min_seg;
     a.defer_merge = plan.defer_merge;
     a.piece_count = a.counters;  // the same scratch region, used one way or the other
+    a.timeout_ns = timeout_ns;
+    a.test_skip_load = skip_load;
     a.status = status;
     return lat::launch_decode_bf16(a, plan.grid, s) == cudaSuccess ? LAT_OK : LAT_ERR_CUDA;
 }
@@ -458,7 +460,8 @@ lat_status lat_attn_decode(lat_dtype dt, const void *q, int64_t q_rs, const void
     return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
                        cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
                        n_kv_heads, head_dim, window, scale, 0.f, 0, workspace,
-                       workspace_bytes, status, stream);
+                       workspace_bytes, status, stream,
+                       kDefaultTimeoutNs, 0);
 }
 
 lat_status lat_attn_decode_ring(lat_dtype dt, const void *q, int64_t q_rs, const void *k_cache,
@@ -473,7 +476,8 @@ lat_status lat_attn_decode_ring(lat_dtype dt, const void *q, int64_t q_rs, const
     return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
                        cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
                        n_kv_heads, head_dim, window, scale, 0.f, ring_capacity, workspace,
-                       workspace_bytes, status, stream);
+                       workspace_bytes, status, stream,
+                       kDefaultTimeoutNs, 0);
 }
 
 lat_status lat_attn_decode_softcap(lat_dtype dt, const void *q, int64_t q_rs,
@@ -487,7 +491,21 @@ lat_status lat_attn_decode_softcap(lat_dtype dt, const void *q, int64_t q_rs,
     return decode_impl(dt, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
                        cache_seq_stride, kv_lens, max_kv_len, out, out_rs, lse, batch, n_heads,
                        n_kv_heads, head_dim, window, scale, softcap, 0, workspace,
-                       workspace_bytes, status, stream);
+                       workspace_bytes, status, stream,
+                       kDefaultTimeoutNs, 0);
+}
+
+lat_status lat_test_decode_timeout(const void *q, int64_t q_rs, const void *k_cache,
+                                   const void *v_cache, int64_t cache_rs,
+                                   int64_t cache_head_stride, int64_t cache_seq_stride,
+                                   const int32_t *kv_lens, int max_kv_len, void *out,
+                                   int64_t out_rs, int batch, int n_heads, int n_kv_heads,
+                                   int head_dim, void *workspace, size_t workspace_bytes,
+                                   uint64_t timeout_ns, int32_t *status, void *stream) {
+    return decode_impl(LAT_BF16, q, q_rs, k_cache, v_cache, cache_rs, cache_head_stride,
+                       cache_seq_stride, kv_lens, max_kv_len, out, out_rs, nullptr, batch,
+                       n_heads, n_kv_heads, head_dim, 0, 0.125f, 0.f, 0, workspace,
+                       workspace_bytes, status, stream, timeout_ns, 1);
 }
 
 }  // extern "C"

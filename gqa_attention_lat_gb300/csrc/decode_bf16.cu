@@ -45,7 +45,6 @@ namespace {
 
 constexpr int kHeadsPerBlock = 8;          // N of the mma: query heads served per unit
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr int kMaxMerges = 2;              // multi-piece units a CTA can finish last
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -233,7 +232,7 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
     }
     fence_proxy_async_smem();  // the scan's generic writes precede the ring's first copies
     __syncthreads();
-    const uint64_t deadline = globaltimer_ns() + kTimeoutNs;
+    const uint64_t deadline = globaltimer_ns() + a.timeout_ns;
     // a deferred merge kernel may be set up now; it waits for this grid before reading
     if (a.defer_merge) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -297,6 +296,10 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                         r.first = t == t0; r.last = t == t1 - 1;
                         r.kq = kq; r.slot = slot; r.nseg = nseg; r.end = 0; r.pad = 0;
                         rec[s] = r;
+                        if (a.test_skip_load && tg == 0) {  // test hook: never filled
+                            ++tg;
+                            continue;
+                        }
                         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                         unsigned char *dk = sRing + s * C::kStageBytes;
                         unsigned char *dv = dk + C::kTileBytes;
@@ -333,7 +336,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
             for (int s = 0; s < C::kStages; ++s)
                 if (s < tg) {
                     const int last = s + (tg - 1 - s) / C::kStages * C::kStages;
-                    mbar_wait_bounded(&full[s], (last / C::kStages) & 1, &no_abort, drain_deadline);
+                    if (!(a.test_skip_load && last == 0))  // the hook's fill was never issued
+                        mbar_wait_bounded(&full[s], (last / C::kStages) & 1, &no_abort, drain_deadline);
                 }
 #pragma unroll
             for (int i = 0; i < 2; ++i)
@@ -737,7 +741,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     // finished and its partial results are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int bh = blockIdx.x / kMergeSplit<D>, cb = blockIdx.x % kMergeSplit<D>;
-    const int nseg = a.piece_count[bh];
+    // (clamped: a stream that gave up early may leave counts of an earlier call)
+    const int nseg = min(a.piece_count[bh], a.max_splits);
     if (nseg <= 1) return;  // written whole by its only piece (or nothing to write)
     const int v0 = cb * kMergeV4<D>, w4 = min(kMergeV4<D>, kV4 - v0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -92,6 +92,8 @@ struct DecodeArgs {
     int defer_merge;
     int32_t *piece_count;  // [batch, n_heads] when defer_merge
     int chunked;           // tm_k/tm_v are chunked 5-D maps: one copy per K or V tile
+    uint64_t timeout_ns;   // budget of every bounded wait, per CTA
+    int test_skip_load;    // test hook: never load a CTA's first K/V stage (forces a timeout)
     int32_t *status;
 };
 struct DecodePlan {

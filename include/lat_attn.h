@@ -169,8 +169,9 @@ size_t lat_attn_decode_workspace_size(lat_dtype dt, int batch, int n_heads, int 
  * (they may hold anything, NaN included).
  * workspace: device scratch of at least lat_attn_decode_workspace_size(...) bytes,
  * 256-byte aligned; it must be zero-filled before its first use with a given layout
- * (the kernel returns its merge counters to zero, so later calls need no reset), and
- * calls sharing one workspace must not overlap on the GPU.  Too small ->
+ * (the kernel returns its merge counters to zero, so later calls need no reset, except
+ * after a call that reported LAT_ERR_TIMEOUT: zero it again), and calls sharing one
+ * workspace must not overlap on the GPU.  Too small ->
  * LAT_ERR_WORKSPACE.  The size depends on the current device's SM count: size the
  * workspace with the device current that will run the call.  LAT_F32 needs no
  * workspace (its size is 0 and the pointer may be NULL).
