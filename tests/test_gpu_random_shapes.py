@@ -5,9 +5,11 @@ Gemma/Qwen shapes, the merge forms).  These cases are drawn from a fixed seed ac
 whole accepted range instead: head_dim 64/80/128/256/512, GQA groups 1-16 (odd ones
 too), ragged query and key counts on either side of the 128-row and 32/64-key tiles,
 causal and bidirectional masks, sliding windows, chunks of new queries after earlier
-keys, packed QKV buffers, the Gemma 2 score cap, and decode batches with empty, short
-and long sequences mixed (both merge forms).  Every output element and lse is compared
-with the fp64 oracle at the tolerances of the other parity tests.
+keys, packed QKV buffers, the Gemma 2 score cap, decode batches with empty, short and
+long sequences mixed (both merge forms), ring caches wrapped up to five times, and KV
+appends into token- and head-major caches in both dtypes.  Every output element and lse
+is compared with the fp64 oracle at the tolerances of the other parity tests; appends
+are compared bit for bit.
 """
 import math
 
@@ -17,7 +19,8 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import DT, DecodeRun, compare, ensure_library, status_tensor
+from gpu_helpers import (DT, DecodeRun, assert_bits_equal, compare, ensure_library,
+                         status_tensor)
 from gqa_attention_lat_gb300 import binding
 
 pytestmark = pytest.mark.gpu
@@ -124,3 +127,93 @@ def test_random_decode_matches_oracle(case):
                                  window=window, scale=scale, softcap=softcap)
     # sequences with no visible key: out = 0, lse = -inf (the oracle's convention)
     compare(out.view(B, Hq, D), ref, "bf16", str(case), lse, ref_lse)
+
+
+def _append_cases(n):
+    rng = np.random.RandomState(SEED + 2)
+    cases = []
+    for _ in range(n):
+        D = int(rng.choice(HEAD_DIMS))
+        Hkv = int(rng.choice((1, 2, 3, 8)))
+        B = int(rng.randint(1, 21))
+        n_new = int(rng.randint(1, 10))
+        cap = n_new + int(rng.randint(0, 400))
+        pos = [int(x) for x in rng.randint(0, cap - n_new + 1, size=B)]
+        dtype = "f32" if rng.rand() < 0.25 else "bf16"
+        head_major = bool(rng.rand() < 0.4)
+        cases.append((B, Hkv, D, cap, n_new, pos, dtype, head_major))
+    return cases
+
+
+APPEND = _append_cases(24)
+
+
+@pytest.mark.parametrize("case", APPEND, ids=lambda c: "B%dHkv%dD%dcap%dT%d-%s%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[6], "-head-major" if c[7] else ""))
+def test_random_append_is_bit_exact(case):
+    """lat_kv_append into NaN-filled caches, token- or head-major, in both dtypes: every
+    cache element equals the oracle's copy, NaN exactly where nothing was written."""
+    B, Hkv, D, cap, n_new, pos, dtype, head_major = case
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    new = W.normal((B * n_new, 2 * Hkv * D), dtype=dtype, device="cuda",
+                   seed=W.BASE_SEED + cap + D, role="new")
+    k_new, v_new = new[:, :Hkv * D], new[:, Hkv * D:]
+    if head_major:  # [B, Hkv, cap, D]
+        kc = torch.full((B, Hkv, cap, D), float("nan"), dtype=tdt, device="cuda")
+        strides = (D, cap * D, Hkv * cap * D)
+    else:           # [B, cap, Hkv, D]
+        kc = torch.full((B, cap, Hkv, D), float("nan"), dtype=tdt, device="cuda")
+        strides = (Hkv * D, D, cap * Hkv * D)
+    vc = torch.full_like(kc, float("nan"))
+    st = status_tensor()
+    binding.lat_kv_append(DT[dtype], kc, vc, strides[0], strides[1], strides[2], cap, k_new,
+                          v_new, new.stride(0), torch.tensor(pos, dtype=torch.int32,
+                                                             device="cuda"),
+                          n_new, B, Hkv, D, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device status %d" % int(st.item())
+    empty = np.full((B, cap, Hkv, D), np.nan)
+    k_rows = k_new.reshape(B, n_new, Hkv, D).float().cpu().numpy()
+    v_rows = v_new.reshape(B, n_new, Hkv, D).float().cpu().numpy()
+    ref_k, ref_v = oracle.kv_append(empty, empty, k_rows, v_rows, pos)
+    got_k = kc.permute(0, 2, 1, 3) if head_major else kc
+    got_v = vc.permute(0, 2, 1, 3) if head_major else vc
+    assert_bits_equal(got_k, ref_k, "K cache")
+    assert_bits_equal(got_v, ref_v, "V cache")
+
+
+def _ring_cases(n):
+    rng = np.random.RandomState(SEED + 3)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice(HEAD_DIMS))
+        Hkv = int(rng.choice((1, 2, 4)))
+        G = int(rng.choice(GROUPS[:6]))
+        B = int(rng.choice((1, 3, 9, 40)))
+        C = int(rng.choice((32, 64, 100, 256, 1024)))
+        Wn = int(rng.randint(1, C + 1))
+        lens = [int(x) for x in rng.randint(0, 5 * C, size=B)]
+        if sum(min(n_, Wn) for n_ in lens) * Hkv * G * D > 3e8:
+            continue
+        cases.append((B, Hkv * G, Hkv, D, C, Wn, lens))
+    return cases
+
+
+RING = _ring_cases(16)
+
+
+@pytest.mark.parametrize("case", RING, ids=lambda c: "B%dH%d-%dD%dC%dW%d" % c[:6])
+def test_random_ring_decode_matches_oracle(case):
+    """Ring caches with the window anywhere up to the ring size, positions up to five
+    wraps, empty sequences among them; rows outside each window hold NaN."""
+    from test_gpu_ring import make_ring, run_ring
+    B, Hq, Hkv, D, C, Wn, lens = case
+    seed = W.BASE_SEED + 11 * C + D
+    kr, vr, kh, vh = make_ring(B, Hkv, D, C, Wn, lens, "bf16", seed)
+    q = W.normal((B, Hq * D), dtype="bf16", device="cuda", seed=seed, role="q")
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    out, lse = run_ring(q, kr, vr, C, lens_t, max(max(lens), 1), B, Hq, Hkv, D, Wn, scale,
+                        "bf16")
+    ref, ref_lse = oracle.decode(q.view(B, Hq, D), kh, vh, lens, window=Wn, scale=scale)
+    compare(out, ref, "bf16", str(case), lse, ref_lse)
