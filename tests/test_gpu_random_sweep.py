@@ -1,19 +1,24 @@
 """Seeded random shapes through prefill and decode, each against the oracle.
 
-The hand-picked sweeps cover the named configurations and their edges; this one draws
-batch, lengths, head counts (GQA group 1..8), head_dim, mask, window, dtype and layout at
-random from a fixed seed, so every run checks the same 64 cases (the next rows' entry
-points included) and a failure is reproducible from its id."""
+The hand-picked sweeps cover the named configurations and their edges; this file draws
+batch, lengths, head counts, head_dim, mask, window, dtype and layout at random from
+fixed seeds, so every run checks the same cases and a failure is reproducible from its
+id.  A first draw (64 cases) includes the next rows' entry points; a second, wider one
+(136 cases) adds GQA groups up to 16 in decode, the score cap on any shape, chunks of new
+queries after earlier keys, ring caches wrapped up to five times, and KV appends into
+token- and head-major caches in both dtypes, compared bit for bit."""
 import math
 import random
 
+import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import compare, ensure_library, oracle_decode, oracle_prefill, run_decode, \
-    run_prefill
+from gpu_helpers import (DT, DecodeRun, assert_bits_equal, compare, ensure_library,
+                         oracle_decode, oracle_prefill, run_decode, run_prefill, status_tensor)
+from gqa_attention_lat_gb300 import binding
 
 pytestmark = pytest.mark.gpu
 
@@ -153,8 +158,6 @@ def test_random_next_rows(case):
         ref, ref_lse = oracle.prefill(inp.heads("q"), inp.heads("k"), inp.heads("v"), causal=True,
                                       window=0, scale=2 * scale, softcap=p["cap"])
     elif kind == "softcap_decode":
-        from gpu_helpers import DT, DecodeRun, status_tensor
-        from gqa_attention_lat_gb300 import binding
         kvcap = p["kvcap"]
         di = W.decode_inputs(B, Hq, Hkv, D, kvcap, kv_lens=p["lens"], dtype=dtype, device="cuda",
                              seed=seed)
@@ -181,3 +184,192 @@ def test_random_next_rows(case):
         out, lse = run_ring(q, kr, vr, C, lens_t, max(lens), B, Hq, Hkv, D, Wn, scale, dtype)
         ref, ref_lse = oracle.decode(q.view(B, Hq, D), kh, vh, lens, window=Wn, scale=scale)
     compare(out, ref, dtype, str(case), lse, ref_lse)
+
+# ---- a second, wider draw (its own seeds): GQA groups up to 16 in decode, the score cap
+# on any shape, ring caches wrapped up to five times, and bit-exact KV appends ----------
+SEED = 20260213
+GROUPS = (1, 2, 3, 4, 5, 8, 16)
+
+
+def _wide_prefill_cases(n):
+    rng = np.random.RandomState(SEED)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice(HEAD_DIMS))
+        Hkv = int(rng.choice((1, 2, 3)))
+        G = int(rng.choice(GROUPS[:5]))
+        B = int(rng.randint(1, 4))
+        S = int(rng.randint(1, 330))
+        packed = bool(rng.rand() < 0.25)
+        L = S if packed or rng.rand() < 0.5 else S + int(rng.randint(1, 300))
+        causal = bool(rng.rand() < 0.75)
+        window = int(rng.randint(1, L + 1)) if rng.rand() < 0.3 else 0
+        softcap = float(rng.choice((1.5, 3.0))) if rng.rand() < 0.2 else 0.0
+        # keep each oracle pass to a fraction of a second
+        if B * S * L * Hkv * G * D > 4e8:
+            continue
+        cases.append((B, S, L, Hkv * G, Hkv, D, causal, window, softcap, packed))
+    return cases
+
+
+def _wide_decode_cases(n):
+    rng = np.random.RandomState(SEED + 1)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice(HEAD_DIMS))
+        Hkv = int(rng.choice((1, 2, 4, 8)))
+        G = int(rng.choice(GROUPS))
+        B = int(rng.choice((1, 2, 3, 7, 16, 40, 64)))
+        cap = int(rng.choice((1, 31, 64, 200, 1000, 4097, 9000)))
+        lens = [int(x) for x in rng.randint(0, cap + 1, size=B)]
+        if rng.rand() < 0.5:
+            lens[int(rng.randint(B))] = cap  # a full-length sequence among them
+        window = int(rng.randint(1, cap + 1)) if rng.rand() < 0.3 else 0
+        softcap = float(rng.choice((1.5, 3.0))) if rng.rand() < 0.2 else 0.0
+        if sum(lens) * Hkv * G * D > 3e9 / 8:
+            continue
+        cases.append((B, Hkv * G, Hkv, D, cap, lens, window, softcap))
+    return cases
+
+
+WIDE_PREFILL = _wide_prefill_cases(48)
+WIDE_DECODE = _wide_decode_cases(48)
+
+
+@pytest.mark.parametrize("case", WIDE_PREFILL, ids=lambda c: "B%dS%dL%dH%d-%dD%d%s%s%s%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], "c" if c[6] else "", "w%d" % c[7] if c[7] else "",
+    "-cap%g" % c[8] if c[8] else "", "-packed" if c[9] else ""))
+def test_wide_random_prefill(case):
+    B, S, L, Hq, Hkv, D, causal, window, softcap, packed = case
+    inp = W.prefill_inputs(B, S, L, Hq, Hkv, D, dtype="bf16", device="cuda", packed=packed,
+                           seed=W.BASE_SEED + 7 * S + L + D)
+    scale = (2.0 if softcap else 1.0) / math.sqrt(D)
+    out = torch.full((B * S, Hq * D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B * S, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    st = status_tensor()
+    binding_args = (DT["bf16"], inp.q, inp.q.stride(0), inp.k, inp.k.stride(0), inp.v,
+                    inp.v.stride(0), out, out.stride(0), lse, B, S, L, Hq, Hkv, D, causal,
+                    window, scale)
+    if softcap:
+        binding.lat_attn_prefill_softcap(*binding_args, softcap, st)
+    else:
+        binding.lat_attn_prefill(*binding_args, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device status %d" % int(st.item())
+    ref, ref_lse = oracle.prefill(inp.heads("q"), inp.heads("k"), inp.heads("v"), causal=causal,
+                                  window=window, scale=scale, softcap=softcap)
+    compare(out.view(B, S, Hq, D), ref, "bf16", str(case), lse.view(B, S, Hq), ref_lse)
+
+
+@pytest.mark.parametrize("case", WIDE_DECODE, ids=lambda c: "B%dH%d-%dD%dcap%d%s%s" % (
+    c[0], c[1], c[2], c[3], c[4], "w%d" % c[6] if c[6] else "", "-cap%g" % c[7] if c[7] else ""))
+def test_wide_random_decode(case):
+    B, Hq, Hkv, D, cap, lens, window, softcap = case
+    di = W.decode_inputs(B, Hq, Hkv, D, cap, kv_lens=lens, device="cuda",
+                         seed=W.BASE_SEED + 3 * cap + D + B)
+    scale = (2.0 if softcap else 1.0) / math.sqrt(D)
+    run = DecodeRun("bf16", B, Hq, Hkv, D, cap)
+    out = torch.full((B, Hq * D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    st = status_tensor()
+    binding.lat_attn_decode_softcap(DT["bf16"], di.q, di.q.stride(0), di.k_cache, di.v_cache,
+                                    Hkv * D, D, cap * Hkv * D, di.kv_lens, cap, out,
+                                    out.stride(0), lse, B, Hq, Hkv, D, window, scale, softcap,
+                                    run.ws, run.nbytes, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device status %d" % int(st.item())
+    ref, ref_lse = oracle.decode(di.q_heads(), di.cache_heads("k_cache"),
+                                 di.cache_heads("v_cache"), di.kv_lens.cpu().tolist(),
+                                 window=window, scale=scale, softcap=softcap)
+    # sequences with no visible key: out = 0, lse = -inf (the oracle's convention)
+    compare(out.view(B, Hq, D), ref, "bf16", str(case), lse, ref_lse)
+
+
+def _append_cases(n):
+    rng = np.random.RandomState(SEED + 2)
+    cases = []
+    for _ in range(n):
+        D = int(rng.choice(HEAD_DIMS))
+        Hkv = int(rng.choice((1, 2, 3, 8)))
+        B = int(rng.randint(1, 21))
+        n_new = int(rng.randint(1, 10))
+        cap = n_new + int(rng.randint(0, 400))
+        pos = [int(x) for x in rng.randint(0, cap - n_new + 1, size=B)]
+        dtype = "f32" if rng.rand() < 0.25 else "bf16"
+        head_major = bool(rng.rand() < 0.4)
+        cases.append((B, Hkv, D, cap, n_new, pos, dtype, head_major))
+    return cases
+
+
+APPEND = _append_cases(24)
+
+
+@pytest.mark.parametrize("case", APPEND, ids=lambda c: "B%dHkv%dD%dcap%dT%d-%s%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[6], "-head-major" if c[7] else ""))
+def test_random_append_is_bit_exact(case):
+    """lat_kv_append into NaN-filled caches, token- or head-major, in both dtypes: every
+    cache element equals the oracle's copy, NaN exactly where nothing was written."""
+    B, Hkv, D, cap, n_new, pos, dtype, head_major = case
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    new = W.normal((B * n_new, 2 * Hkv * D), dtype=dtype, device="cuda",
+                   seed=W.BASE_SEED + cap + D, role="new")
+    k_new, v_new = new[:, :Hkv * D], new[:, Hkv * D:]
+    if head_major:  # [B, Hkv, cap, D]
+        kc = torch.full((B, Hkv, cap, D), float("nan"), dtype=tdt, device="cuda")
+        strides = (D, cap * D, Hkv * cap * D)
+    else:           # [B, cap, Hkv, D]
+        kc = torch.full((B, cap, Hkv, D), float("nan"), dtype=tdt, device="cuda")
+        strides = (Hkv * D, D, cap * Hkv * D)
+    vc = torch.full_like(kc, float("nan"))
+    st = status_tensor()
+    binding.lat_kv_append(DT[dtype], kc, vc, strides[0], strides[1], strides[2], cap, k_new,
+                          v_new, new.stride(0), torch.tensor(pos, dtype=torch.int32,
+                                                             device="cuda"),
+                          n_new, B, Hkv, D, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device status %d" % int(st.item())
+    empty = np.full((B, cap, Hkv, D), np.nan)
+    k_rows = k_new.reshape(B, n_new, Hkv, D).float().cpu().numpy()
+    v_rows = v_new.reshape(B, n_new, Hkv, D).float().cpu().numpy()
+    ref_k, ref_v = oracle.kv_append(empty, empty, k_rows, v_rows, pos)
+    got_k = kc.permute(0, 2, 1, 3) if head_major else kc
+    got_v = vc.permute(0, 2, 1, 3) if head_major else vc
+    assert_bits_equal(got_k, ref_k, "K cache")
+    assert_bits_equal(got_v, ref_v, "V cache")
+
+
+def _ring_cases(n):
+    rng = np.random.RandomState(SEED + 3)
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice(HEAD_DIMS))
+        Hkv = int(rng.choice((1, 2, 4)))
+        G = int(rng.choice(GROUPS[:6]))
+        B = int(rng.choice((1, 3, 9, 40)))
+        C = int(rng.choice((32, 64, 100, 256, 1024)))
+        Wn = int(rng.randint(1, C + 1))
+        lens = [int(x) for x in rng.randint(0, 5 * C, size=B)]
+        if sum(min(n_, Wn) for n_ in lens) * Hkv * G * D > 3e8:
+            continue
+        cases.append((B, Hkv * G, Hkv, D, C, Wn, lens))
+    return cases
+
+
+RING = _ring_cases(16)
+
+
+@pytest.mark.parametrize("case", RING, ids=lambda c: "B%dH%d-%dD%dC%dW%d" % c[:6])
+def test_wide_random_ring_decode(case):
+    """Ring caches with the window anywhere up to the ring size, positions up to five
+    wraps, empty sequences among them; rows outside each window hold NaN."""
+    from test_gpu_ring import make_ring, run_ring
+    B, Hq, Hkv, D, C, Wn, lens = case
+    seed = W.BASE_SEED + 11 * C + D
+    kr, vr, kh, vh = make_ring(B, Hkv, D, C, Wn, lens, "bf16", seed)
+    q = W.normal((B, Hq * D), dtype="bf16", device="cuda", seed=seed, role="q")
+    lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    out, lse = run_ring(q, kr, vr, C, lens_t, max(max(lens), 1), B, Hq, Hkv, D, Wn, scale,
+                        "bf16")
+    ref, ref_lse = oracle.decode(q.view(B, Hq, D), kh, vh, lens, window=Wn, scale=scale)
+    compare(out, ref, "bf16", str(case), lse, ref_lse)
