@@ -409,7 +409,13 @@ lat_status decode_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k_
                                  cache_head_stride, cache_seq_stride, box) &&
                       make_cache_map(&a.tm_v, v_cache, head_dim, n_kv_heads, rows, batch,
                                      cache_rs, cache_head_stride, cache_seq_stride, box);
-        if (!maps_ok || !make_query_map(&a.tm_q, q, head_dim, n_heads, batch, q_rs))
+        const bool partial_ok =
+            make_cache_map(&a.tm_k16, k_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
+                           cache_head_stride, cache_seq_stride, 16) &&
+            make_cache_map(&a.tm_v16, v_cache, head_dim, n_kv_heads, rows, batch, cache_rs,
+                           cache_head_stride, cache_seq_stride, 16);
+        if (!maps_ok || !partial_ok ||
+            !make_query_map(&a.tm_q, q, head_dim, n_heads, batch, q_rs))
             return LAT_ERR_CUDA;
     }
     a.q = static_cast<const __nv_bfloat16 *>(q);

@@ -241,6 +241,8 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
         if (lane == 0) {
             tma_prefetch_desc(&a.tm_k);
             tma_prefetch_desc(&a.tm_v);
+            tma_prefetch_desc(&a.tm_k16);
+            tma_prefetch_desc(&a.tm_v16);
             tma_prefetch_desc(&a.tm_q);
             int tg = 0, kq = 0;  // stage fills issued, query blocks issued
             bool ok = true;
@@ -300,9 +302,27 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
                             ++tg;
                             continue;
                         }
-                        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                         unsigned char *dk = sRing + s * C::kStageBytes;
                         unsigned char *dv = dk + C::kTileBytes;
+                        const int rows_valid = kend - key0;  // > 0: the part's rows in the tile
+                        if (rows_valid < T) {
+                            // a part's partial last tile: only its 16-row groups that hold
+                            // keys, each landing where the whole tile would put those rows
+                            // (rows past them are masked in S and zeroed in V as before)
+                            const int nb = (rows_valid + 15) / 16;
+                            mbar_arrive_expect_tx(&full[s], 2 * C::kCols64 * nb * 16 * 128);
+                            for (int c = 0; c < C::kCols64; ++c)
+                                for (int i = 0; i < nb; ++i) {
+                                    const uint32_t off = c * C::kTile * 128 + i * 16 * 128;
+                                    tma_load_4d(dk + off, &a.tm_k16, &full[s], c * 64, hk,
+                                                key0 + 16 * i, b);
+                                    tma_load_4d(dv + off, &a.tm_v16, &full[s], c * 64, hk,
+                                                key0 + 16 * i, b);
+                                }
+                            ++tg;
+                            continue;
+                        }
+                        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                         if (a.chunked) {  // each tile's 64-column chunks in one copy
                             tma_load_5d(dk, &a.tm_k, &full[s], 0, key0, 0, hk, b);
                             tma_load_5d(dv, &a.tm_v, &full[s], 0, key0, 0, hk, b);

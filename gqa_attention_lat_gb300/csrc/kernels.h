@@ -67,6 +67,7 @@ cudaError_t launch_row_attention_f32(const RowAttnArgs &a, cudaStream_t s);
 // ---------------------------------------------------------------- bf16 split-KV decode
 struct DecodeArgs {
     CUtensorMap tm_k, tm_v;  // 4-D maps (d, head, row < max_kv_len, sequence), 128-byte swizzle
+    CUtensorMap tm_k16, tm_v16;  // the same with 16-row boxes: a sequence's partial last tile
     CUtensorMap tm_q;        // 3-D map (d, query head, sequence), 8-head boxes, 128-byte swizzle
     const __nv_bfloat16 *q;
     int64_t q_rs;
