@@ -17,12 +17,15 @@
 //    streams its share without draining its pipeline between units; a unit cut across
 //    CTAs leaves one partial (normalised output and log-sum-exp) per piece, merged by
 //    the CTA that finishes the unit's last piece (an atomic ticket), after its stream.
-//  * One producer thread streams K and V tiles with TMA (4-D tensor maps over the cache's
-//    (head-dim, head, row, sequence) strides, 128-byte swizzled 64-column chunks) into a
-//    ring of stages, each tagged with a record of what it holds; each unit's query rows
-//    arrive by TMA into a double buffer.  Rows past a piece's end are masked in S and, on
-//    its ragged last tile, zeroed in V by the warp that owns them (cache slots there may
-//    hold NaN).
+//    With few units (one long sequence, say) the stream is cut across every CTA and a
+//    second kernel, launched as a programmatic dependent, merges the pieces instead.
+//  * One producer thread streams K and V tiles with TMA (tensor maps over the cache's
+//    (head-dim, head, row, sequence) strides, 128-byte swizzled 64-column chunks: one
+//    copy per K or V tile where head_dim is 64-256, a copy per chunk at 512, and a part's
+//    partial last tile in 16-row boxes) into a ring of stages, each tagged with a record
+//    of what it holds; each unit's query rows arrive by TMA into a double buffer.  Rows
+//    past a piece's end are masked in S and zeroed in V by the warp that owns them
+//    (cache slots there may hold NaN).
 //  * The contraction runs on the tensor cores with keys in the M dimension:
 //      S^T[16 keys x 8 heads]   = K[16 x D] . Q^T[D x 8]        (mma m16n8k16)
 //      O^T[D x 8 heads]        += V^T[D x 16 keys] . P^T[16 x 8]
@@ -30,8 +33,10 @@
 //    S^T's accumulator by an in-register 8x8 transpose (movmatrix).
 //  * Each warp owns 16 keys of every tile and keeps its own running max/sum, refreshed
 //    only when the max grows by more than 2^8 (so the O rescale is rare); at the end of
-//    a piece the warps' states meet in shared memory and warp 0 writes the result.
-//  * Every wait is bounded; on expiry the CTA records LAT_ERR_TIMEOUT and quits.
+//    a piece the warps park their states in shared memory and each combines a share of
+//    the heads from all of them and writes it out.
+//  * Every wait is bounded (the budget comes with the launch); on expiry the CTA records
+//    LAT_ERR_TIMEOUT, drains its copies and quits.
 #include <math.h>
 
 #include <algorithm>
