@@ -93,15 +93,17 @@ struct TcCfg {
     static constexpr int kVChunkBytes = kBN * 128;
     static constexpr int kKTileBytes = kQkChunks * kKChunkBytes;
     static constexpr int kVTileBytes = kVChunks * kVChunkBytes;
-    // head_dim 64 keeps few tiles in flight: its tiles are small and its per-tile chain is
-    // set by the softmax, and with deeper rings (4 K + 4 V slots and a second query tile)
-    // every CTA's requests queue behind one another, so each load lands later (measured:
-    // 2 + 2 slots and one query tile 25.7 vs 26.5 us on the Qwen3 shape; 1 + 1 slots for
-    // the 96-key tiles 70.1 vs 75.2 us on the chunked prefill)
-    static constexpr int kKStages = P ? 1 : (D == 64 ? (W ? 1 : 2) : (D <= 128 ? 3 : 1));
-    static constexpr int kVStages = P ? 1 : (D == 64 ? (W ? 1 : 2) : (D <= 128 ? 2 : 1));
+    // Few tiles in flight: with deeper rings (and the next item's query tile loaded ahead)
+    // every CTA's requests queue behind one another and each load lands later, while the
+    // per-tile chain is set by the MMAs and the softmax.  Measured: head_dim 64, 2 + 2
+    // slots and one query tile 25.7 vs 26.5 us (4 + 4 and two) on the Qwen3 shape, 1 + 1
+    // for the 96-key tiles 70.1 vs 75.2 us (3 + 3) on the chunked prefill; head_dim 128,
+    // 1 + 1 and one query tile 555.8 vs 574.0 us (3 + 2 and two) on B1 S8192 H32/8 and
+    // 49.5 vs 51.4 us on B8 S512.
+    static constexpr int kKStages = D == 64 && !W ? 2 : 1;
+    static constexpr int kVStages = D == 64 && !W ? 2 : 1;
     static constexpr int kQBytes = kQkChunks * kBM * 128;
-    static constexpr int kQStages = D == 128 || D == 80 ? 2 : 1;  // the next item's Q loads early
+    static constexpr int kQStages = 1;
     static constexpr int kBarBytes = 256 + 4 * kBM * 4;  // barriers + row exchange
     static constexpr int kPayload = kQStages * kQBytes + kKStages * kKTileBytes +
                                     kVStages * kVTileBytes + kBarBytes;
