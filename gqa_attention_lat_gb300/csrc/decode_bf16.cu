@@ -58,12 +58,12 @@ struct DecodeCfg {
     static constexpr int kWarps = D >= 256 ? 2 : 4;           // compute warps
     static constexpr int kThreads = 32 * (kWarps + 1);        // + one producer warp
     static constexpr int kTile = 16 * kWarps;                 // keys per pipeline stage
-    // head_dim 64-128: two stages measured as fast as three on the ragged 32-sequence decode
-    // at head_dim 128 and 4 % faster on one long sequence, and 4.5 % faster than four at
-    // head_dim 64 (B32 H16/8 at up to 4096 keys): every CTA's first stages are requested at
-    // once and land sooner when there are fewer.  head_dim 256/512 keep three (two were
-    // slower there).
-    static constexpr int kStages = D <= 128 ? 2 : 3;
+    // Two stages up to head_dim 256: as fast as three on the ragged 32-sequence decode at
+    // head_dim 128 and on the ring decode at 256, and faster where every CTA's first stages
+    // dominate (one long sequence at 128: 4 %; B32 H16/8 up to 4096 keys: 4.5 % at head_dim
+    // 64 against four stages, 2.7 % at 256): requested all at once, fewer land sooner.
+    // head_dim 512 (one CTA per SM) needs its three 64 KB stages (two: 3 % slower).
+    static constexpr int kStages = D == 512 ? 3 : 2;
     static constexpr int kMinBlocks = D == 512 ? 1 : (D == 64 ? 3 : 2);  // CTAs per SM
     static constexpr int kChunks = D / 8;                     // 16-byte chunks per row
     static constexpr int kCols64 = (D + 63) / 64;             // 64-column TMA chunks per row
