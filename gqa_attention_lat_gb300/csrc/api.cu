@@ -110,6 +110,25 @@ bool make_query_map(CUtensorMap *m, const void *base, int head_dim, int heads, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over a prefill output: (column < heads * head_dim, row < rows, batch) with
+// 32-row boxes of box_cols columns, swizzled to the box's row width (128 or 64 bytes).
+// Stores clip at the row extent, so rows past a sequence's end are never written.
+bool make_out_map(CUtensorMap *m, void *base, int head_dim, int heads, int rows, int batch,
+                  int64_t row_stride, int box_cols) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr || (box_cols != 64 && box_cols != 32)) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)heads * (cuuint64_t)head_dim, (cuuint64_t)rows,
+                                (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2,
+                                   (cuuint64_t)row_stride * 2 * (cuuint64_t)rows};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int current_sm_count(int *out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -209,8 +228,13 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
         !make_cache_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, kv.v_row, kv.v_head,
                         kv.v_seq, v_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return LAT_ERR_CUDA;
+    const int out_box = lat::prefill_tc_out_box_cols(head_dim);
+    if (out_box > 0 && !a.pair &&
+        !make_out_map(&a.tm_out, out, head_dim, n_heads, seq_len, batch, out_rs, out_box))
+        return LAT_ERR_CUDA;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.out_rs = out_rs;
+    a.out_v8 = reinterpret_cast<uintptr_t>(out) % 32 == 0 && out_rs % 16 == 0;
     a.lse = lse;
     a.batch = batch;
     a.seq_len = seq_len;

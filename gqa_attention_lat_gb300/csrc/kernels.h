@@ -114,8 +114,12 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, int grid, cudaStream_t s);
 // ---------------------------------------------------------------- bf16 tensor-core prefill
 struct PrefillTcArgs {
     CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps (d, head, row, batch), 128-byte swizzle
+    // 3-D map over the output (column, row < seq_len, batch), 32-row boxes of
+    // prefill_tc_out_box_cols columns; used where that is nonzero
+    CUtensorMap tm_out;
     __nv_bfloat16 *out;
     int64_t out_rs;
+    int out_v8;                    // out and out_rs allow 32-byte row stores
     float *lse;
     int batch, seq_len, kv_len, n_heads, n_kv_heads, head_dim, causal, window;
     float scale_log2;              // scale * log2(e)
@@ -139,6 +143,8 @@ int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v);
 // forms that move each tile in one copy through chunked 5-D maps, and the 64-column
 // chunks of one V copy
 bool prefill_tc_chunked(int head_dim, bool pair);
+// columns of one output box where the epilogue stores through tm_out, else 0
+int prefill_tc_out_box_cols(int head_dim);
 int prefill_tc_v_chunks(int head_dim, bool pair);
 // work items of one prefill launch (query tile x head x output-column part); the kernel
 // numbers them in int32, so the host refuses shapes above kPrefillMaxItems

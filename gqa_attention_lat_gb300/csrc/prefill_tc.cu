@@ -104,9 +104,23 @@ struct TcCfg {
     static constexpr int kVStages = D == 64 && !W ? 2 : 1;
     static constexpr int kQBytes = kQkChunks * kBM * 128;
     static constexpr int kQStages = 1;
+    // Output staging (single-CTA head_dim 128/256): each softmax warp writes its 32 rows x
+    // kEpiCols output columns per pass into one of its kEpiBufs swizzled boxes and hands the
+    // box to one TMA store.  Row-per-thread global stores touch 32 rows per instruction, and
+    // at head_dim 256 they held the softmax warps for most of a 3 us item boundary.  Head_dim
+    // 64 (two stores per thread), 80 (no whole boxes) and 512 (no shared memory left) store
+    // rows directly.
+    static constexpr bool kEpiTma = !P && (D == 128 || D == 256);
+    static constexpr int kEpiCols = 64;                                   // box columns
+    static constexpr int kEpiBufs = 1;                                    // boxes per warp
+    static constexpr int kEpiPasses = kEpiTma ? D / 2 / kEpiCols : 0;     // boxes per item
+    static constexpr int kEpiBoxBytes = 32 * kEpiCols * 2;
+    static constexpr int kEpiBytes =
+        kEpiTma ? kSoftmaxThreads / 32 * kEpiBufs * kEpiBoxBytes : 0;
+    static_assert(!kEpiTma || 2 * kEpiPasses * kEpiCols == D, "boxes cover the head");
     static constexpr int kBarBytes = 256 + 4 * kBM * 4;  // barriers + row exchange
     static constexpr int kPayload = kQStages * kQBytes + kKStages * kKTileBytes +
-                                    kVStages * kVTileBytes + kBarBytes;
+                                    kVStages * kVTileBytes + kEpiBytes + kBarBytes;
     // 1 KB of slack lets the 1024-byte aligned carve-up start anywhere; a shape that
     // cannot afford it relies on the dynamic shared memory base being 1024-byte aligned
     // (checked at run time)
@@ -226,7 +240,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     unsigned char *sQ = smem;                                 // [kQStages] Q tiles
     unsigned char *sK = sQ + C::kQStages * C::kQBytes;        // [kKStages] K tiles
     unsigned char *sV = sK + C::kKStages * C::kKTileBytes;    // [kVStages] V tiles
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sV + C::kVStages * C::kVTileBytes);
+    unsigned char *sEpi = sV + C::kVStages * C::kVTileBytes;  // output boxes, one per warp
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::kEpiBytes);
     uint64_t *q_full = bars + 0;       // [2]
     uint64_t *q_empty = bars + 2;      // [2]
     uint64_t *bar_s = bars + 4;        // [2] S(g) ready, by global tile parity
@@ -674,7 +689,50 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             __nv_bfloat16 *orow = a.out + qrow * a.out_rs + (int64_t)it.h * D + it.half * C::kOCols;
             const bool empty = !(l_sum > 0.f);
             const float inv_l = empty ? 0.f : 1.f / l_sum;
-            if (n_tiles > 0) {
+            if constexpr (C::kEpiTma) {
+                // warpgroup wg takes output columns [wg * D/2, (wg + 1) * D/2), one box of
+                // kEpiCols per pass: lane r writes row r of the box (16-byte pieces placed
+                // by the swizzle the map expects), then lane 0 stores the box.  Rows past
+                // the sequence end fall outside the map and are not written.
+                constexpr uint32_t kRowBytes = C::kEpiCols * 2;   // 128 or 64
+                constexpr uint32_t kSwMask = kRowBytes / 16 - 1;  // 128- or 64-byte swizzle
+                unsigned char *boxes = sEpi + warp * C::kEpiBufs * C::kEpiBoxBytes;
+                const uint32_t row_off = (uint32_t)lane * kRowBytes;
+                const uint32_t sw = (row_off >> 7) & kSwMask;
+#pragma unroll 1
+                for (int ps = 0; ps < C::kEpiPasses; ++ps) {
+                    unsigned char *box = boxes + (ps % C::kEpiBufs) * C::kEpiBoxBytes;
+                    const uint32_t my_row = smem_u32(box) + row_off;
+                    const int c0 = wg * (D / 2) + ps * C::kEpiCols;
+                    uint32_t pk[C::kEpiCols / 2];
+                    if (n_tiles > 0) {
+                        uint32_t ov[C::kEpiCols];
+#pragma unroll
+                        for (int c = 0; c < C::kEpiCols; c += 16)
+                            tmem_ld16(lane_base + kTmemO + c0 + c, ov + c);  // warp-wide
+                        tc_wait_ld();
+#pragma unroll
+                        for (int kk = 0; kk < C::kEpiCols / 2; ++kk)
+                            pk[kk] = pack_bf16x2(__uint_as_float(ov[2 * kk]) * inv_l,
+                                                 __uint_as_float(ov[2 * kk + 1]) * inv_l);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < C::kEpiCols / 2; ++kk) pk[kk] = 0u;
+                    }
+                    if (lane == 0) bulk_wait_read<C::kEpiBufs - 1>();  // the box is free again
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < (int)(kRowBytes / 16); ++j)
+                        st_shared_v4(my_row + (((uint32_t)j ^ sw) << 4), pk[4 * j],
+                                     pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_smem();  // the generic writes before the async read
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&a.tm_out, box, it.h * D + c0, it.m0 + quarter * 32, it.b);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (n_tiles > 0) {
 #pragma unroll 1
                 for (int c = 16 * wg; c < C::kOCols; c += 32) {
                     uint32_t ov[16];
@@ -686,9 +744,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                         pk[kk] = pack_bf16x2(__uint_as_float(ov[2 * kk]) * inv_l,
                                              __uint_as_float(ov[2 * kk + 1]) * inv_l);
                     if (live) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        if (a.out_v8) {
+                            st_global_v8(orow + c, pk);
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+                            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        }
                     }
                 }
             } else if (live) {
@@ -700,6 +762,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     empty ? -INFINITY : (m_ref + log2f(l_sum)) * 0.69314718055994531f;
             // the O reads above complete before this thread's next P is published, and the
             // next item's first P.V (which overwrites O) waits for that P
+        }
+        if constexpr (C::kEpiTma) {
+            if (lane == 0) bulk_wait_all();  // output stores done before shared memory goes
         }
     }
 
@@ -797,6 +862,14 @@ int prefill_tc_block_n(int head_dim, bool wide) {
 int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v) {
     if (pair) return v ? TcCfg<512, false, true>::kBN : TcCfg<512, false, true>::kKRows;
     return prefill_tc_block_n(head_dim, wide);
+}
+
+int prefill_tc_out_box_cols(int head_dim) {
+    switch (head_dim) {
+        case 128: return TcCfg<128>::kEpiCols;
+        case 256: return TcCfg<256>::kEpiCols;
+        default: return 0;
+    }
 }
 
 bool prefill_tc_chunked(int head_dim, bool pair) {

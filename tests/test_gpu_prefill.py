@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import workloads as W
-from gpu_helpers import compare, ensure_library, oracle_prefill, run_prefill
+from gpu_helpers import compare, ensure_library, oracle_prefill, run_prefill, status_tensor
+from gqa_attention_lat_gb300 import binding
 
 pytestmark = pytest.mark.gpu
 
@@ -161,3 +162,36 @@ def test_prefill_many_short_sequences():
     out, lse = run_prefill(inp, causal=True, window=0, scale=0.125)
     ref, ref_lse = oracle_prefill(inp, causal=True, window=0, scale=0.125)
     compare(out, ref, "bf16", "300 x 37 rows", lse, ref_lse)
+
+
+# Output placement: short ragged sequences (every query tile ends inside its sequence, and
+# the next sequence's rows follow at once), an output that is a column window of a wider
+# buffer starting 0 or 16 bytes past a 32-byte boundary, and rows after the last sequence.
+# Rows and columns outside the window must keep their sentinel.  Covers the tensor-map
+# output stores (head_dim 128/256) and the direct row stores in their 32- and 16-byte forms.
+@pytest.mark.parametrize("D,Hq,Hkv,col0", [
+    (64, 4, 2, 0), (64, 4, 2, 8), (80, 4, 2, 0), (80, 4, 2, 8), (128, 4, 2, 0), (128, 4, 1, 8),
+    (256, 3, 1, 0), (256, 2, 2, 8), (512, 4, 2, 0), (512, 4, 2, 8), (512, 3, 1, 0),
+], ids=lambda v: str(v))
+def test_prefill_output_stays_in_its_window(D, Hq, Hkv, col0):
+    B, S = 5, 37
+    inp = W.prefill_inputs(B, S, S, Hq, Hkv, D, dtype="bf16", device="cuda",
+                           seed=W.BASE_SEED + 11 * D + col0)
+    rows, width, tail = B * S, Hq * D, 40
+    # row strides of 16-element multiples (col0 0) and of 8 (col0 8)
+    full = torch.full((rows + tail, col0 + width + (24 if col0 else 32)), float("nan"),
+                      dtype=torch.bfloat16, device="cuda")
+    out = full[:rows, col0:col0 + width]
+    lse = torch.full((rows, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    st = status_tensor()
+    binding.lat_attn_prefill(binding.LAT_BF16, inp.q, inp.q.stride(0), inp.k, inp.k.stride(0),
+                             inp.v, inp.v.stride(0), out, out.stride(0), lse, B, S, S, Hq, Hkv,
+                             D, True, 0, 0.1, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    outside = torch.ones_like(full, dtype=torch.bool)
+    outside[:rows, col0:col0 + width] = False
+    assert torch.isnan(full[outside].float()).all(), "prefill wrote outside its output"
+    ref, ref_lse = oracle_prefill(inp, causal=True, window=0, scale=0.1)
+    compare(out.reshape(B, S, Hq, D), ref, "bf16", "D%d col0 %d" % (D, col0),
+            lse.reshape(B, S, Hq), ref_lse)
