@@ -228,8 +228,8 @@ lat_status prefill_impl(lat_dtype dt, const void *q, int64_t q_rs, const void *k
         !make_cache_map(&a.tm_v, v, head_dim, n_kv_heads, kv_len, batch, kv.v_row, kv.v_head,
                         kv.v_seq, v_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return LAT_ERR_CUDA;
-    const int out_box = lat::prefill_tc_out_box_cols(head_dim);
-    if (out_box > 0 && !a.pair &&
+    const int out_box = lat::prefill_tc_out_box_cols(head_dim, a.pair != 0);
+    if (out_box > 0 &&
         !make_out_map(&a.tm_out, out, head_dim, n_heads, seq_len, batch, out_rs, out_box))
         return LAT_ERR_CUDA;
     a.out = static_cast<__nv_bfloat16 *>(out);

@@ -144,7 +144,7 @@ int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v);
 // chunks of one V copy
 bool prefill_tc_chunked(int head_dim, bool pair);
 // columns of one output box where the epilogue stores through tm_out, else 0
-int prefill_tc_out_box_cols(int head_dim);
+int prefill_tc_out_box_cols(int head_dim, bool pair);
 int prefill_tc_v_chunks(int head_dim, bool pair);
 // work items of one prefill launch (query tile x head x output-column part); the kernel
 // numbers them in int32, so the host refuses shapes above kPrefillMaxItems

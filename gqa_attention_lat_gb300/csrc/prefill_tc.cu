@@ -104,20 +104,26 @@ struct TcCfg {
     static constexpr int kVStages = D == 64 && !W ? 2 : 1;
     static constexpr int kQBytes = kQkChunks * kBM * 128;
     static constexpr int kQStages = 1;
-    // Output staging (single-CTA head_dim 128/256): each softmax warp writes its 32 rows x
-    // kEpiCols output columns per pass into one of its kEpiBufs swizzled boxes and hands the
-    // box to one TMA store.  Row-per-thread global stores touch 32 rows per instruction, and
-    // at head_dim 256 they held the softmax warps for most of a 3 us item boundary.  Head_dim
-    // 64 (two stores per thread), 80 (no whole boxes) and 512 (no shared memory left) store
-    // rows directly.
-    static constexpr bool kEpiTma = !P && (D == 128 || D == 256);
+    // Output staging: each softmax warp writes its 32 rows x kEpiCols output columns per
+    // pass into one of its kEpiBufs swizzled boxes and hands the box to one TMA store.
+    // Row-per-thread global stores touch 32 rows per instruction, and at head_dim 256 they
+    // held the softmax warps for most of a 3 us item boundary.  Single-CTA head_dim 128/256
+    // stage in boxes of their own; the CTA pair (no shared memory left) stages in its V
+    // slot, which is free from the item's last P.V until the next item's first V copy, and
+    // that copy waits until the boxes have been read.  Head_dim 64 (two stores per thread),
+    // 80 (no whole boxes) and single-CTA 512 (no room) store rows directly.
+    static constexpr bool kEpiOwn = !P && (D == 128 || D == 256);
+    static constexpr bool kEpiInV = P;
+    static constexpr bool kEpiTma = kEpiOwn || kEpiInV;
     static constexpr int kEpiCols = 64;                                   // box columns
     static constexpr int kEpiBufs = 1;                                    // boxes per warp
-    static constexpr int kEpiPasses = kEpiTma ? D / 2 / kEpiCols : 0;     // boxes per item
+    static constexpr int kEpiPasses = kEpiTma ? kOCols / 2 / kEpiCols : 0;  // boxes per item
     static constexpr int kEpiBoxBytes = 32 * kEpiCols * 2;
-    static constexpr int kEpiBytes =
-        kEpiTma ? kSoftmaxThreads / 32 * kEpiBufs * kEpiBoxBytes : 0;
-    static_assert(!kEpiTma || 2 * kEpiPasses * kEpiCols == D, "boxes cover the head");
+    static constexpr int kEpiStageBytes = kSoftmaxThreads / 32 * kEpiBufs * kEpiBoxBytes;
+    static constexpr int kEpiBytes = kEpiOwn ? kEpiStageBytes : 0;
+    static_assert(!kEpiTma || 2 * kEpiPasses * kEpiCols == kOCols, "boxes cover the columns");
+    static_assert(!kEpiInV || (kVStages == 1 && kEpiStageBytes <= kVTileBytes),
+                  "the boxes fit the V slot");
     static constexpr int kBarBytes = 256 + 4 * kBM * 4;  // barriers + row exchange
     static constexpr int kPayload = kQStages * kQBytes + kKStages * kKTileBytes +
                                     kVStages * kVTileBytes + kEpiBytes + kBarBytes;
@@ -242,6 +248,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     unsigned char *sV = sK + C::kKStages * C::kKTileBytes;    // [kVStages] V tiles
     unsigned char *sEpi = sV + C::kVStages * C::kVTileBytes;  // output boxes, one per warp
     uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + C::kEpiBytes);
+    unsigned char *sStage = C::kEpiInV ? sV : sEpi;            // where the boxes are staged
     uint64_t *q_full = bars + 0;       // [2]
     uint64_t *q_empty = bars + 2;      // [2]
     uint64_t *bar_s = bars + 4;        // [2] S(g) ready, by global tile parity
@@ -254,7 +261,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
     uint64_t *k_empty = k_full + C::kKStages;
     uint64_t *v_full = k_empty + C::kKStages;   // [kVStages]
     uint64_t *v_empty = v_full + C::kVStages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(v_empty + C::kVStages);
+    uint64_t *epi_done = v_empty + C::kVStages;  // one phase per item: its boxes are read
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *xchg = reinterpret_cast<float *>(bars + 32);   // [2 parities][2 warpgroups][kBM]
 
@@ -280,6 +288,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
         mbar_init(bar_o, 1);
         mbar_init(o_full, 1);
         mbar_init(bar_done, 1);
+        mbar_init(epi_done, kSoftmaxThreads / 32);  // one arrival per softmax warp
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -340,6 +349,12 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                 const int idx = item_index(k, cta, G, n_items);
                 if (idx < 0) break;
                 const Item it = item_at<D, W, P>(a, idx, rank);
+                // the V slot held the previous item's output boxes until their stores read them
+                if (C::kEpiInV && !is_k && k > 0 &&
+                    !mbar_wait_bounded(epi_done, (k - 1) & 1, abort_flag, deadline)) {
+                    ok = false;
+                    break;
+                }
                 if (is_k) {
                     const int qs = qi % C::kQStages;
                     if (!wait_bar(&q_empty[qs], ((qi / C::kQStages) & 1) ^ 1)) {
@@ -690,20 +705,20 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
             const bool empty = !(l_sum > 0.f);
             const float inv_l = empty ? 0.f : 1.f / l_sum;
             if constexpr (C::kEpiTma) {
-                // warpgroup wg takes output columns [wg * D/2, (wg + 1) * D/2), one box of
+                // warpgroup wg takes O columns [wg, wg + 1) * kOCols / 2, one box of
                 // kEpiCols per pass: lane r writes row r of the box (16-byte pieces placed
                 // by the swizzle the map expects), then lane 0 stores the box.  Rows past
                 // the sequence end fall outside the map and are not written.
                 constexpr uint32_t kRowBytes = C::kEpiCols * 2;   // 128 or 64
                 constexpr uint32_t kSwMask = kRowBytes / 16 - 1;  // 128- or 64-byte swizzle
-                unsigned char *boxes = sEpi + warp * C::kEpiBufs * C::kEpiBoxBytes;
+                unsigned char *boxes = sStage + warp * C::kEpiBufs * C::kEpiBoxBytes;
                 const uint32_t row_off = (uint32_t)lane * kRowBytes;
                 const uint32_t sw = (row_off >> 7) & kSwMask;
 #pragma unroll 1
                 for (int ps = 0; ps < C::kEpiPasses; ++ps) {
                     unsigned char *box = boxes + (ps % C::kEpiBufs) * C::kEpiBoxBytes;
                     const uint32_t my_row = smem_u32(box) + row_off;
-                    const int c0 = wg * (D / 2) + ps * C::kEpiCols;
+                    const int c0 = wg * (C::kOCols / 2) + ps * C::kEpiCols;  // O column
                     uint32_t pk[C::kEpiCols / 2];
                     if (n_tiles > 0) {
                         uint32_t ov[C::kEpiCols];
@@ -728,8 +743,19 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                     fence_proxy_async_smem();  // the generic writes before the async read
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&a.tm_out, box, it.h * D + c0, it.m0 + quarter * 32, it.b);
+                        tma_store_3d(&a.tm_out, box, it.h * D + it.half * C::kOCols + c0,
+                                     it.m0 + quarter * 32, it.b);
                         bulk_commit_group();
+                    }
+                }
+                // hand the V slot back once the boxes are read.  Every item visits at least
+                // one key tile (kv_len >= seq_len), so the V producer, which waits for each
+                // item's boxes before the next item's first V copy, never falls two phases
+                // behind this barrier.
+                if constexpr (C::kEpiInV) {
+                    if (lane == 0) {
+                        bulk_wait_read<0>();
+                        mbar_arrive(epi_done);
                     }
                 }
             } else if (n_tiles > 0) {
@@ -864,7 +890,8 @@ int prefill_tc_box_rows(int head_dim, bool wide, bool pair, bool v) {
     return prefill_tc_block_n(head_dim, wide);
 }
 
-int prefill_tc_out_box_cols(int head_dim) {
+int prefill_tc_out_box_cols(int head_dim, bool pair) {
+    if (pair) return TcCfg<512, false, true>::kEpiCols;
     switch (head_dim) {
         case 128: return TcCfg<128>::kEpiCols;
         case 256: return TcCfg<256>::kEpiCols;
