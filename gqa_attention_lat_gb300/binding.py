@@ -66,6 +66,7 @@ _SIGNATURES = {
                                         _I32, _I32, _I32, _U64, _P, _P]),
     "lat_test_decode_timeout": (_I32, [_P, _I64, _P, _P, _I64, _I64, _I64, _P, _I32, _P, _I64,
                                        _I32, _I32, _I32, _I32, _P, _SZ, _U64, _P, _P]),
+    "lat_test_capped_scores": (_I32, [_P, _I64, _F32, _F32, _P, _P]),
 }
 
 
@@ -237,3 +238,8 @@ def lat_test_decode_timeout(q, q_rs, k_cache, v_cache, cache_rs, cache_head_stri
         cache_seq_stride, _ptr(kv_lens), max_kv_len, _ptr(out), out_rs, batch, n_heads,
         n_kv_heads, head_dim, _ptr(workspace), workspace_bytes, timeout_ns, _ptr(status),
         _stream(stream)), "lat_test_decode_timeout")
+
+
+def lat_test_capped_scores(raw, n, scale, softcap, out, stream=None):
+    _check(library().lat_test_capped_scores(_ptr(raw), n, scale, softcap, _ptr(out),
+                                            _stream(stream)), "lat_test_capped_scores")

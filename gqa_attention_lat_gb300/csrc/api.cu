@@ -538,6 +538,18 @@ lat_status lat_test_decode_timeout(const void *q, int64_t q_rs, const void *k_ca
                        workspace_bytes, status, stream, timeout_ns, 1);
 }
 
+lat_status lat_test_capped_scores(const float *raw, int64_t n, float scale, float softcap,
+                                  float *out, void *stream) {
+    if (n < 0 || !(softcap > 0.f) || !isfinite(scale)) return LAT_ERR_INVALID_ARG;
+    if (n == 0) return LAT_OK;
+    if (raw == nullptr || out == nullptr) return LAT_ERR_INVALID_ARG;
+    // the same two factors the attention entry points hand their kernels
+    return lat::launch_capped_scores(raw, n, scale / softcap, softcap * kLog2e, out,
+                                     static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? LAT_OK
+               : LAT_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace {

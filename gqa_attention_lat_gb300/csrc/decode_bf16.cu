@@ -454,8 +454,9 @@ decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
             }
             // scale (and cap) into the log2 domain and mask keys past the piece
             if (a.cap_log2 > 0.f) {
+                const float k2 = a.raw_over_cap * kTwoLog2e;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[e] = a.cap_log2 * tanhf(sc[e] * a.raw_over_cap);
+                for (int e = 0; e < 4; ++e) sc[e] = capped_score_log2(sc[e], k2, a.cap_log2);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[e] *= a.scale_log2;

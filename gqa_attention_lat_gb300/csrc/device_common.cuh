@@ -237,6 +237,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// 2 log2(e): e^{2y} = 2^{y * kTwoLog2e}
+constexpr float kTwoLog2e = 2.8853900817779268f;
+
+// Score cap in the log2 domain: cap_log2 * tanh(y) for y = raw * raw_over_cap, from the
+// identity tanh y = 1 - 2 / (1 + e^{2y}), with e^{2y} = 2^{raw * k2} (k2 = raw_over_cap *
+// kTwoLog2e) from the hardware exp2 and the quotient from a reciprocal and a multiply.
+// The error is absolute, a few 1e-7 of tanh over the whole range (near y = 0 the form
+// subtracts two numbers close to 1, which costs relative but not absolute accuracy, and
+// the score is cap_log2 * tanh); y -> +inf gives e^{2y} = inf and 2 / inf = 0, so exactly
+// cap_log2, and y -> -inf exactly -cap_log2.
+__device__ __forceinline__ float capped_score_log2(float raw, float k2, float cap_log2) {
+    return cap_log2 - __fdividef(2.f * cap_log2, 1.f + fast_exp2(raw * k2));
+}
+
 // ------------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
 

@@ -151,5 +151,8 @@ int prefill_tc_v_chunks(int head_dim, bool pair);
 int64_t prefill_tc_items(int batch, int n_heads, int head_dim, int seq_len);
 constexpr int64_t kPrefillMaxItems = int64_t(1) << 30;
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t s);
+// out[i] = the capped score (log2 domain) of raw[i], as the bf16 kernels form it
+cudaError_t launch_capped_scores(const float *raw, int64_t n, float raw_over_cap,
+                                 float cap_log2, float *out, cudaStream_t s);
 
 }  // namespace lat

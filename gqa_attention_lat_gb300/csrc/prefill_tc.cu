@@ -591,8 +591,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                               reinterpret_cast<uint32_t *>(sv + c));
                 tc_wait_ld();
                 if (capped) {  // Gemma 2 score cap, in the log2 domain
+                    const float k2 = a.raw_over_cap * kTwoLog2e;
 #pragma unroll
-                    for (int c = 0; c < HC; ++c) sv[c] = a.cap_log2 * tanhf(sv[c] * a.raw_over_cap);
+                    for (int c = 0; c < HC; ++c) sv[c] = capped_score_log2(sv[c], k2, a.cap_log2);
                 }
 
                 const int key0 = (it.band.t_begin + t) * BN;
@@ -934,6 +935,23 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, int num_sms, cudaStream_t 
         case 512: return launch_d<512>(a, num_sms, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// the score cap alone, for testing it against tanh (grid-stride over n values)
+__global__ void capped_scores_kernel(const float *raw, int64_t n, float raw_over_cap,
+                                     float cap_log2, float *out) {
+    const float k2 = raw_over_cap * kTwoLog2e;  // formed as the attention kernels form it
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = capped_score_log2(raw[i], k2, cap_log2);
+}
+
+cudaError_t launch_capped_scores(const float *raw, int64_t n, float raw_over_cap,
+                                 float cap_log2, float *out, cudaStream_t s) {
+    const int64_t blocks = (n + 255) / 256;
+    capped_scores_kernel<<<(int)(blocks < 1184 ? blocks : 1184), 256, 0, s>>>(
+        raw, n, raw_over_cap, cap_log2, out);
+    return cudaGetLastError();
 }
 
 }  // namespace lat

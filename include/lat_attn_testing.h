@@ -17,6 +17,13 @@
  * kernel, if the shape uses one, still runs and finishes.  Arguments, layout and
  * workspace rules are those of lat_attn_decode; the output is unspecified, and the
  * workspace must be zero-filled again before its next use.
+ *
+ * lat_test_capped_scores evaluates the score cap of the bf16 kernels (the Gemma 2 softcap
+ * of the larql "BLAS-Fused Attention" step 2, folded into the log2 domain) on n raw dot
+ * products: out[i] = softcap * log2(e) * tanh(raw[i] * scale / softcap), formed exactly as
+ * lat_attn_prefill_softcap and lat_attn_decode_softcap form it.  raw and out are device
+ * arrays of n floats (n >= 0) that do not overlap; softcap > 0 and scale finite, else
+ * LAT_ERR_INVALID_ARG.  Asynchronous on `stream`.
  */
 #ifndef LAT_ATTN_TESTING_H
 #define LAT_ATTN_TESTING_H
@@ -39,6 +46,8 @@ lat_status lat_test_decode_timeout(const void *q, int64_t q_rs, const void *k_ca
                                    int64_t out_rs, int batch, int n_heads, int n_kv_heads,
                                    int head_dim, void *workspace, size_t workspace_bytes,
                                    uint64_t timeout_ns, int32_t *status, void *stream);
+lat_status lat_test_capped_scores(const float *raw, int64_t n, float scale, float softcap,
+                                  float *out, void *stream);
 
 #ifdef __cplusplus
 }

@@ -106,3 +106,44 @@ def test_decode_softcap_matches_oracle(case):
                                  di.cache_heads("v_cache"), di.kv_lens.cpu().tolist(),
                                  window=window, scale=scale, softcap=softcap)
     compare(out.view(B, Hq, D), ref, dtype, str(case), lse, ref_lse)
+
+
+# The bf16 kernels form the capped score as cap * log2(e) * tanh(y) through
+# tanh y = 1 - 2 / (1 + e^{2y}) with the hardware exp2; its error is absolute, a few 1e-7
+# of tanh.  Checked against the exact value (fp64 tanh of the same fp32 factors) and
+# against CUDA's own tanhf (torch.tanh on the device), over raw dot products from 1e-30 to
+# 1e30, both signs, zero and the infinities (which must give exactly +-cap * log2(e)).
+@pytest.mark.parametrize("scale,softcap", [(0.0625, 50.0), (0.0884, 30.0), (1.0, 2.0),
+                                           (0.5, 1e-3)])
+def test_capped_score_matches_tanh(scale, softcap):
+    g = torch.Generator().manual_seed(W.BASE_SEED + 77)
+    parts = [torch.randn(50000, generator=g, dtype=torch.float64) * s
+             for s in (1e-3, 0.1, 1.0, 30.0, 300.0, 3000.0)]
+    parts.append(torch.tensor([0.0, 1e-30, -1e-30, 1e-7, -1e-7, 1e30, -1e30]))
+    raw = torch.cat(parts).float()
+    special = torch.tensor([math.inf, -math.inf])
+    raw_all = torch.cat([raw, special]).cuda()
+    out = torch.full_like(raw_all, math.nan)
+    binding.lat_test_capped_scores(raw_all, raw_all.numel(), scale, softcap, out)
+    torch.cuda.synchronize()
+    raw_over_cap = np.float32(np.float32(scale) / np.float32(softcap))
+    cap_log2 = np.float32(np.float32(softcap) * np.float32(1.4426950408889634))
+    y64 = raw.double() * float(raw_over_cap)
+    exact = float(cap_log2) * torch.tanh(y64)
+    got = out[:-2].cpu().double()
+    bound = 1e-6 * float(cap_log2)
+    err = (got - exact).abs().max().item()
+    assert err <= bound, "capped score off by %.3g (bound %.3g)" % (err, bound)
+    cuda_tanh = float(cap_log2) * torch.tanh(raw.cuda() * raw_over_cap.item()).cpu().double()
+    err_cuda = (got - cuda_tanh).abs().max().item()
+    assert err_cuda <= bound, "capped score vs tanhf off by %.3g" % err_cuda
+    assert out[-2].item() == pytest.approx(float(cap_log2), abs=0.0)
+    assert out[-1].item() == pytest.approx(-float(cap_log2), abs=0.0)
+    assert torch.isfinite(out).all()
+
+
+def test_capped_score_rejects_bad_arguments():
+    x = torch.zeros(4, device="cuda")
+    for scale, softcap in [(0.1, 0.0), (0.1, -1.0), (math.inf, 5.0), (math.nan, 5.0)]:
+        with pytest.raises(Exception):
+            binding.lat_test_capped_scores(x, 4, scale, softcap, x)
