@@ -88,3 +88,24 @@ def test_prefill_cached_equals_prefill_on_contiguous_kv():
     torch.cuda.synchronize()
     assert torch.equal(out_a.view(B, S, Hq, D), out_b)
     assert torch.equal(lse_a.view(B, S, Hq), lse_b)
+
+
+def test_chunked_prefill_workload_full_sampled_rows():
+    """The measured chunked prefill at full size (B8, 512 new rows after 1536 cached keys,
+    Hq16/8 D64, a 4096-slot token-major cache whose slots past L hold NaN; the bench's own
+    inputs), in its 96-key-tile form: sampled rows against the oracle."""
+    wl = W.WORKLOADS["qwen3_chunked_prefill"]
+    di = W.decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.cap, kv_lens=wl.L, dtype=wl.dtype,
+                         device="cuda", nan_fill=True)
+    q = W.normal((wl.B * wl.S, wl.Hq * wl.D), dtype=wl.dtype, device="cuda", seed=W.BASE_SEED,
+                 role="chunk_q")
+    out, lse = run_cached(q, di.k_cache, di.v_cache, wl.Hkv * wl.D, wl.D,
+                          wl.cap * wl.Hkv * wl.D, wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D,
+                          wl.causal, wl.window, wl.scale, wl.dtype)
+    rows = W.sample_rows(wl.B * wl.S, wl.S, extra=[95, 96, 127, 128, 255, 256], n_random=256)
+    kt, vt = di.cache_heads("k_cache"), di.cache_heads("v_cache")
+    ref, ref_lse = oracle.prefill(q.view(wl.B, wl.S, wl.Hq, wl.D), kt[:, :wl.L], vt[:, :wl.L],
+                                  causal=wl.causal, window=wl.window, scale=wl.scale, rows=rows)
+    idx = torch.tensor(rows, device="cuda")
+    compare(out.reshape(wl.B * wl.S, wl.Hq, wl.D)[idx], ref, wl.dtype, wl.name,
+            lse.reshape(wl.B * wl.S, wl.Hq)[idx], ref_lse)

@@ -149,3 +149,27 @@ def test_ring_append_bit_exact(dtype, head_major):
                                        vn.view(B, n_new, Hkv, D).cpu().float().numpy(), pos)
     assert_bits_equal(as_rows(kc), ok_k, "K ring")
     assert_bits_equal(as_rows(vc), ok_v, "V ring")
+
+
+def test_ring_decode_workload_full():
+    """The measured ring workload at full size (B32 Hq16/8 D256, a 1024-row ring, window
+    1024, absolute lengths up to 32768, the bench's own inputs): every output against the
+    oracle over each sequence's visible positions gathered from the ring in order."""
+    wl = W.WORKLOADS["gemma4_sliding_decode_ring"]
+    di = W.ring_decode_inputs(wl.B, wl.Hq, wl.Hkv, wl.D, wl.ring, wl.max_len, dtype=wl.dtype,
+                              device="cuda")
+    out, lse = run_ring(di.q, di.k_cache, di.v_cache, wl.ring, di.kv_lens, wl.max_len, wl.B,
+                        wl.Hq, wl.Hkv, wl.D, wl.window, wl.scale, wl.dtype)
+    lens = di.kv_lens.cpu().tolist()
+    vis = [min(n, wl.window) for n in lens]
+    kr = di.k_cache.cpu().view(wl.B, wl.ring, wl.Hkv, wl.D)
+    vr = di.v_cache.cpu().view(wl.B, wl.ring, wl.Hkv, wl.D)
+    kl = torch.zeros((wl.B, max(vis), wl.Hkv, wl.D), dtype=kr.dtype)
+    vl = torch.zeros_like(kl)
+    for b, (n, m) in enumerate(zip(lens, vis)):
+        rows = torch.tensor([p % wl.ring for p in range(n - m, n)])
+        kl[b, :m] = kr[b, rows]
+        vl[b, :m] = vr[b, rows]
+    ref, ref_lse = oracle.decode(di.q.cpu().view(wl.B, wl.Hq, wl.D), kl, vl, vis, window=0,
+                                 scale=wl.scale)
+    compare(out, ref, wl.dtype, wl.name, lse, ref_lse)

@@ -147,3 +147,20 @@ def test_capped_score_rejects_bad_arguments():
     for scale, softcap in [(0.1, 0.0), (0.1, -1.0), (math.inf, 5.0), (math.nan, 5.0)]:
         with pytest.raises(Exception):
             binding.lat_test_capped_scores(x, 4, scale, softcap, x)
+
+
+def test_softcap_prefill_workload_full_sampled_rows():
+    """The measured capped prefill at full size (B1 S8192 Hq16/8 D256, cap 50, the bench's
+    own inputs): sampled rows (sequence ends, tile boundaries, random rows) against the
+    oracle's fp64 tanh."""
+    wl = W.WORKLOADS["gemma2_softcap_prefill"]
+    inp = W.prefill_inputs(wl.B, wl.S, wl.L, wl.Hq, wl.Hkv, wl.D, dtype=wl.dtype, device="cuda",
+                           packed=wl.packed, k_mul=wl.k_mul)
+    out, lse = run_prefill_softcap(inp, wl.causal, wl.window, wl.scale, wl.softcap)
+    rows = W.sample_rows(wl.B * wl.S, wl.S, extra=[127, 128, 4095, 4096], n_random=256)
+    ref, ref_lse = oracle.prefill(inp.heads("q"), inp.heads("k"), inp.heads("v"),
+                                  causal=wl.causal, window=wl.window, scale=wl.scale, rows=rows,
+                                  softcap=wl.softcap)
+    idx = torch.tensor(rows, device="cuda")
+    compare(out.reshape(wl.B * wl.S, wl.Hq, wl.D)[idx], ref, wl.dtype, wl.name,
+            lse.reshape(wl.B * wl.S, wl.Hq)[idx], ref_lse)
