@@ -710,8 +710,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillTcArgs a) {
                 // kEpiCols per pass: lane r writes row r of the box (16-byte pieces placed
                 // by the swizzle the map expects), then lane 0 stores the box.  Rows past
                 // the sequence end fall outside the map and are not written.
-                constexpr uint32_t kRowBytes = C::kEpiCols * 2;   // 128 or 64
-                constexpr uint32_t kSwMask = kRowBytes / 16 - 1;  // 128- or 64-byte swizzle
+                constexpr uint32_t kRowBytes = C::kEpiCols * 2;   // bytes per box row
+                constexpr uint32_t kSwMask = kRowBytes / 16 - 1;  // the swizzle of that width
                 unsigned char *boxes = sStage + warp * C::kEpiBufs * C::kEpiBoxBytes;
                 const uint32_t row_off = (uint32_t)lane * kRowBytes;
                 const uint32_t sw = (row_off >> 7) & kSwMask;
