@@ -142,6 +142,7 @@ def test_gemma4_prefill_sampled_rows(name):
     (1, 32768, 4, 1, 128, 0),
     (1, 20000, 8, 2, 64, 0),      # head_dim 64 in its 96-key-tile form
     (1, 16384, 4, 2, 256, 4096),
+    (1, 131072, 8, 1, 128, 0),    # 128K rows: tile coordinates and item counts at scale
 ], ids=lambda c: "S%dH%d-%dD%dw%d" % (c[1], c[2], c[3], c[4], c[5]))
 def test_prefill_long_sequence_sampled_rows(case):
     B, S, Hq, Hkv, D, window = case
@@ -149,7 +150,8 @@ def test_prefill_long_sequence_sampled_rows(case):
                            seed=W.BASE_SEED + S + D)
     scale = 1.0 / math.sqrt(D)
     out, lse = run_prefill(inp, causal=True, window=window, scale=scale)
-    rows = W.sample_rows(B * S, S, extra=[127, 128, 4095, 4096, S // 2], n_random=256)
+    rows = W.sample_rows(B * S, S, extra=[127, 128, 4095, 4096, S // 2],
+                         n_random=256 if S <= 32768 else 24)
     ref, ref_lse = oracle_prefill(inp, causal=True, window=window, scale=scale, rows=rows)
     idx = torch.tensor(rows, device="cuda")
     compare(out.reshape(B * S, Hq, D)[idx], ref, "bf16", str(case),
