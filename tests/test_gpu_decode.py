@@ -255,3 +255,13 @@ def test_decode_large_batch_with_empty_sequences():
     compare(out, ref, "bf16", "B600 with empty sequences", lse, ref_lse)
     empty = (lens == 0).nonzero().flatten().tolist()
     assert empty and torch.all(out[empty].float() == 0)
+
+
+def test_decode_million_keys():
+    """Key streams past 2^20: two sequences, 1048576 and 700001 cached keys (slots past
+    each length NaN), every output against the oracle."""
+    di = W.decode_inputs(2, 8, 1, 128, 1 << 20, kv_lens=[1 << 20, 700001], dtype="bf16",
+                         device="cuda", seed=W.BASE_SEED + 21)
+    out, lse = run_decode(di, window=0, scale=1.0 / math.sqrt(128))
+    ref, ref_lse = oracle_decode(di, window=0, scale=1.0 / math.sqrt(128))
+    compare(out, ref, "bf16", "1M keys", lse, ref_lse)
